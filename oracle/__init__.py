@@ -1,0 +1,223 @@
+"""fp64 host oracle for the tensor-parallel sharded linear layer and MLP block.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
+``__graft_entry__.py`` and the CPU-baseline / reference arm of ``bench.py``
+may import this package.  The CUDA library never calls it and it never calls
+the CUDA library; the two share only the seeded input generator, which holds
+none of the method's arithmetic.
+
+The arithmetic lives in ``oracle.c`` (plain loops, double accumulation); this
+module only compiles it with the host C compiler, loads it and marshals numpy
+arrays.  Every function states the passage it follows:
+
+* [TP-topic]  chipfoundryservices.com topic page "Tensor Parallelism":
+  "Tensor Parallelism Fundamentals", "Column-Wise Parallelism",
+  "Row-Wise Parallelism", "Megatron-LM Tensor Parallelism", SVG figure panel
+  "Attention Head Parallelism".
+* [Glossary]  aiforbusinessandlife.com glossary "Tensor Parallelism":
+  "How it works", "Worked example", "Check your understanding".
+
+Readings taken where the pages are silent or garbled (each is also listed in
+the design notes):
+
+* Row split: the Fundamentals bullet prints the per-device product as
+  "X_i.W"; the Row-Wise section and the worked example split the contracted
+  dimension of both X and W, Y_i = X_i.W_i.  The latter is used.
+* Combine after a column split is a concat (Column-Wise section, glossary
+  worked example); the figure's "all-reduce" box belongs to the MLP pair.
+* The activation is the exact GeLU, x*Phi(x), with the host libm erf.
+* Partials are summed in ascending shard order.
+* Head-group split for the QKV projection: columns form G blocks (Q|K|V) and
+  shard i owns the i-th contiguous slice of each block.
+
+Parity pins for each function are in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_fp = ctypes.POINTER(ctypes.c_float)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with the host C compiler.
+
+    Portable flags only (no -march=native): the library may be built on one
+    host and run on another.  No -ffast-math, so every double operation is
+    IEEE round-to-nearest and no sum is reassociated.
+    """
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.orc_matmul.argtypes = [_dp, _dp, _dp, _i64, _i64, _i64]
+        lib.orc_gelu.argtypes = [ctypes.c_double]
+        lib.orc_gelu.restype = ctypes.c_double
+        lib.orc_gelu_inplace.argtypes = [_dp, _i64]
+        lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_to_double.restype = ctypes.c_double
+        lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.orc_bf16_from_double.restype = ctypes.c_uint16
+        lib.orc_bf16_to_double_array.argtypes = [_u16p, _dp, _i64]
+        lib.orc_double_to_bf16_array.argtypes = [_dp, _u16p, _i64]
+        lib.orc_column_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                          _i64, _i64, ctypes.c_int]
+        lib.orc_row_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
+        lib.orc_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
+                                      ctypes.c_int]
+        lib.orc_shard_reduce.argtypes = [_fp, _dp, _i64, _i64, _i64]
+        lib.orc_shard_concat.argtypes = [_dp, _dp, _i64, _i64, _i64, _i64]
+        _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray, typ=_dp):
+    return a.ctypes.data_as(typ) if a is not None else None
+
+
+def set_threads(n: int) -> None:
+    """Number of host threads the OpenMP loops use (row-parallel only)."""
+    os.environ["OMP_NUM_THREADS"] = str(int(n))
+    try:
+        libgomp = ctypes.CDLL("libgomp.so.1")
+        libgomp.omp_set_num_threads(ctypes.c_int(int(n)))
+    except OSError:
+        pass
+
+
+# ----------------------------------------------------------------- bf16 -----
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact double values (format definition)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().orc_bf16_to_double_array(_ptr(b, _u16p), _ptr(out), b.size)
+    return out
+
+
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """double -> bf16 bit patterns, round to nearest, ties to even."""
+    a = _f64(x)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().orc_double_to_bf16_array(_ptr(a), _ptr(out, _u16p), a.size)
+    return out
+
+
+# ----------------------------------------------------------------- maths ----
+
+def gelu(x) -> np.ndarray:
+    """Exact GeLU x*Phi(x) applied elementwise ([TP-topic] Megatron-LM, MLP
+    layer splitting: the activation is applied to each shard independently)."""
+    a = _f64(x).copy()
+    _load().orc_gelu_inplace(_ptr(a), a.size)
+    return a
+
+
+def matmul(X, W) -> np.ndarray:
+    """Unsharded Y = X.W ([TP-topic] Fundamentals), naive loops in double."""
+    X, W = _f64(X), _f64(W)
+    M, K = X.shape
+    K2, N = W.shape
+    assert K == K2
+    Y = np.empty((M, N), dtype=np.float64)
+    _load().orc_matmul(_ptr(X), _ptr(W), _ptr(Y), M, K, N)
+    return Y
+
+
+def column_linear(X, W, n_shards: int, col_groups: int = 1, act: str | None = None):
+    """Column-parallel linear ([TP-topic] "Column-Wise Parallelism").
+
+    Returns (Y, Ys): the concatenated output [M, N] and the shard-major local
+    outputs [n_shards, M, N/n_shards].  ``act='gelu'`` applies the exact GeLU
+    to each shard's output before the concat.
+    """
+    X, W = _f64(X), _f64(W)
+    M, K = X.shape
+    _, N = W.shape
+    assert N % col_groups == 0 and (N // col_groups) % n_shards == 0
+    Y = np.empty((M, N), dtype=np.float64)
+    Ys = np.empty((n_shards, M, N // n_shards), dtype=np.float64)
+    _load().orc_column_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(Ys), M, K, N,
+                              n_shards, col_groups, 1 if act == "gelu" else 0)
+    return Y, Ys
+
+
+def row_linear(X, W, n_shards: int):
+    """Row-parallel linear ([TP-topic] "Row-Wise Parallelism").
+
+    Returns (Y, P): Y = sum of the shard partials (ascending shard order) and
+    the partials P [n_shards, M, N].
+    """
+    X, W = _f64(X), _f64(W)
+    M, K = X.shape
+    _, N = W.shape
+    assert K % n_shards == 0
+    Y = np.empty((M, N), dtype=np.float64)
+    P = np.empty((n_shards, M, N), dtype=np.float64)
+    _load().orc_row_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(P), M, K, N, n_shards)
+    return Y, P
+
+
+def mlp_block(X, W1, W2, n_shards: int, mirror_h_bf16: bool = False) -> np.ndarray:
+    """Megatron-style MLP block ([TP-topic] Megatron-LM, "MLP Layer Splitting"):
+    Y = sum_i GeLU(X.W1_i).W2_i with W1 split by columns and W2 by rows."""
+    X, W1, W2 = _f64(X), _f64(W1), _f64(W2)
+    M, d = X.shape
+    _, f = W1.shape
+    assert W2.shape == (f, d) and f % n_shards == 0
+    Y = np.empty((M, d), dtype=np.float64)
+    _load().orc_mlp_block(_ptr(X), _ptr(W1), _ptr(W2), _ptr(Y), M, d, f, n_shards,
+                          1 if mirror_h_bf16 else 0)
+    return Y
+
+
+def shard_reduce(P) -> np.ndarray:
+    """Sum of fp32 partials [n, rows, cols] over ascending shard, in double."""
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    n, rows, cols = P.shape
+    Y = np.empty((rows, cols), dtype=np.float64)
+    _load().orc_shard_reduce(_ptr(P, _fp), _ptr(Y), rows, cols, n)
+    return Y
+
+
+def shard_concat(Ys, col_groups: int = 1) -> np.ndarray:
+    """Concat of shard outputs [n, rows, sc] into [rows, n*sc] (column
+    ownership as in column_linear)."""
+    Ys = _f64(Ys)
+    n, rows, sc = Ys.shape
+    assert sc % col_groups == 0
+    Y = np.empty((rows, n * sc), dtype=np.float64)
+    _load().orc_shard_concat(_ptr(Ys), _ptr(Y), rows, sc, n, col_groups)
+    return Y

@@ -1,0 +1,283 @@
+/*
+ * oracle.c -- fp64 host oracle for the tensor-parallel sharded linear layer
+ * and the Megatron-style MLP block built from it.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * and the bench's CPU-baseline / reference arm load this library.  It shares
+ * no code, header, table or helper with the CUDA path.
+ *
+ * Every routine is the plain definition written out: naive loops, double
+ * accumulation, no blocking, no fusion, no reordering beyond what the
+ * definition states.  The only liberty taken is running independent output
+ * rows on several host threads (OpenMP), which does not change any sum.
+ *
+ * Sources (web pages on tensor parallelism; see the Python wrapper for the
+ * list of readings taken where the pages are silent):
+ *   [TP-topic]  chipfoundryservices.com, "Tensor Parallelism" topic page:
+ *               "Tensor Parallelism Fundamentals", "Column-Wise Parallelism",
+ *               "Row-Wise Parallelism", "Megatron-LM Tensor Parallelism",
+ *               and the SVG figure's "Attention Head Parallelism" panel.
+ *   [Glossary]  aiforbusinessandlife.com glossary "Tensor Parallelism":
+ *               "How it works" and "Worked example".
+ *
+ * All matrices are row-major.  Y = X W with X [M,K], W [K,N], Y [M,N].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* The unsharded linear map.                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Y[M,N] = X[M,K] . W[K,N]  ([TP-topic] Fundamentals, "Y = XW").
+ * y[i][j] = sum over k = 0..K-1, in ascending k, of x[i][k] * w[k][j]. */
+void orc_matmul(const double *X, const double *W, double *Y,
+                int64_t M, int64_t K, int64_t N)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double *y = Y + i * N;
+        for (int64_t j = 0; j < N; ++j)
+            y[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double x = X[i * K + k];
+            const double *w = W + k * N;
+            for (int64_t j = 0; j < N; ++j)
+                y[j] += x * w[j];
+        }
+    }
+}
+
+/* Exact GeLU: x * Phi(x), Phi the standard normal CDF.  The pages only say
+ * an activation is applied to each shard with no exchange ([TP-topic]
+ * Megatron-LM, "MLP Layer Splitting"); the exact (erf) GeLU is the reading
+ * taken for every MLP block.  Phi(x) = (1 + erf(x/sqrt 2))/2 is evaluated as
+ * erfc(-x/sqrt 2)/2 (the same function; host libm erfc), which keeps full
+ * relative precision in the negative tail where 1 + erf cancels. */
+double orc_gelu(double x)
+{
+    return x * (0.5 * erfc(-x / sqrt(2.0)));
+}
+
+void orc_gelu_inplace(double *v, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        v[i] = orc_gelu(v[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> double, written from the format's definition:                   */
+/* 1 sign bit, 8 exponent bits (bias 127, same range as IEEE binary32),     */
+/* 7 stored significand bits; rounding to nearest, ties to even.            */
+/* ------------------------------------------------------------------------ */
+
+double orc_bf16_to_double(uint16_t b)
+{
+    const int sign = (b >> 15) & 1;
+    const int e = (b >> 7) & 0xFF;
+    const int m = b & 0x7F;
+    double v;
+    if (e == 0xFF)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -126 - 7);           /* subnormal: m * 2^-133 */
+    else
+        v = ldexp((double)(128 + m), e - 127 - 7); /* 1.m * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+uint16_t orc_bf16_from_double(double x)
+{
+    const uint16_t s = signbit(x) ? 0x8000 : 0;
+    if (isnan(x))
+        return (uint16_t)(s | 0x7FC0);
+    double a = fabs(x);
+    /* The midpoint between the largest finite value (2-2^-7)*2^127 and 2^128
+     * rounds to the even neighbour, 2^128, which is out of range. */
+    const double overflow_mid = ldexp(2.0 - ldexp(1.0, -8), 127);
+    if (a >= overflow_mid)
+        return (uint16_t)(s | 0x7F80);
+    if (a == 0.0)
+        return s;
+    int e2;
+    frexp(a, &e2);              /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;             /* a = 1.xxx * 2^E */
+    if (E < -126)
+        E = -126;               /* subnormal range shares the quantum 2^-133 */
+    const double q = ldexp(1.0, E - 7);
+    const double r = nearbyint(a / q); /* a/q is exact; default mode = ties to even */
+    /* r in [0, 256].  For normals r in [128, 256]; r == 256 carries into the
+     * exponent.  For subnormals r in [0, 128]; r == 128 is the smallest normal.
+     * Both cases are covered by adding r to the biased exponent field. */
+    uint32_t bits = (uint32_t)((E + 127 - 1) << 7) + (uint32_t)r;
+    if (bits >= 0x7F80)
+        return (uint16_t)(s | 0x7F80);
+    return (uint16_t)(s | bits);
+}
+
+void orc_bf16_to_double_array(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = orc_bf16_to_double(src[i]);
+}
+
+void orc_double_to_bf16_array(const double *src, uint16_t *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = orc_bf16_from_double(src[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Column-parallel linear ([TP-topic] "Column-Wise Parallelism"; [Glossary]  */
+/* "How it works": splitting W by output columns gives different columns    */
+/* of Y, which are concatenated).                                            */
+/*                                                                           */
+/* W = [W_0, ..., W_{n-1}]; shard i computes Y_i = X . W_i; Y = concat(Y_i). */
+/*                                                                           */
+/* With col_groups G > 1 the output columns form G equal blocks (for an      */
+/* attention QKV projection: Q | K | V) and shard i owns the i-th slice of   */
+/* every block -- the head-group split of the SVG figure's "Attention Head   */
+/* Parallelism" panel, where each device owns a subset of heads.  With       */
+/* gw = N/G and sw = gw/n, shard i owns columns {b*gw + i*sw + j}, b < G,    */
+/* j < sw, and its local output is [M, G*sw] ordered block by block.         */
+/* ------------------------------------------------------------------------ */
+void orc_column_linear(const double *X, const double *W, double *Y, double *Ys,
+                       int64_t M, int64_t K, int64_t N, int64_t n_shards,
+                       int64_t col_groups, int act_gelu)
+{
+    const int64_t gw = N / col_groups;
+    const int64_t sw = gw / n_shards;
+    const int64_t nl = col_groups * sw;
+    double *Wi = (double *)malloc(sizeof(double) * (size_t)(K * nl > 0 ? K * nl : 1));
+    double *Yi = (double *)malloc(sizeof(double) * (size_t)(M * nl > 0 ? M * nl : 1));
+    for (int64_t i = 0; i < n_shards; ++i) {
+        /* the shard's weight block, copied out as a separate matrix */
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t b = 0; b < col_groups; ++b)
+                for (int64_t j = 0; j < sw; ++j)
+                    Wi[k * nl + b * sw + j] = W[k * N + b * gw + i * sw + j];
+        orc_matmul(X, Wi, Yi, M, K, nl);
+        if (act_gelu)
+            orc_gelu_inplace(Yi, M * nl);       /* per shard, no exchange */
+        /* all-gather: place the shard's columns into the full output */
+        if (Y)
+            for (int64_t r = 0; r < M; ++r)
+                for (int64_t b = 0; b < col_groups; ++b)
+                    for (int64_t j = 0; j < sw; ++j)
+                        Y[r * N + b * gw + i * sw + j] = Yi[r * nl + b * sw + j];
+        if (Ys)
+            memcpy(Ys + i * M * nl, Yi, sizeof(double) * (size_t)(M * nl));
+    }
+    free(Wi);
+    free(Yi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row-parallel linear ([TP-topic] "Row-Wise Parallelism": W stacked         */
+/* vertically [W_0; ...; W_{n-1}], X split to match, Y_i = X_i . W_i,       */
+/* Y = sum_i Y_i; [Glossary] "Worked example": splitting the contracted      */
+/* dimension gives partial contributions that are added).                    */
+/*                                                                           */
+/* Shard i owns rows [i*K/n, (i+1)*K/n) of W and the same columns of X.     */
+/* The partials are summed in ascending shard order.  P, if given, receives */
+/* the partials as [n, M, N].                                                */
+/* ------------------------------------------------------------------------ */
+void orc_row_linear(const double *X, const double *W, double *Y, double *P,
+                    int64_t M, int64_t K, int64_t N, int64_t n_shards)
+{
+    const int64_t ks = K / n_shards;
+    double *Xi = (double *)malloc(sizeof(double) * (size_t)(M * ks > 0 ? M * ks : 1));
+    double *Pi = (double *)malloc(sizeof(double) * (size_t)(M * N > 0 ? M * N : 1));
+    for (int64_t t = 0; t < M * N; ++t)
+        Y[t] = 0.0;
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t k = 0; k < ks; ++k)
+                Xi[r * ks + k] = X[r * K + i * ks + k];
+        /* W_i is a contiguous block of rows of W: rows i*ks .. i*ks+ks-1 */
+        orc_matmul(Xi, W + i * ks * N, Pi, M, ks, N);
+        /* all-reduce: add this shard's partial */
+        for (int64_t t = 0; t < M * N; ++t)
+            Y[t] += Pi[t];
+        if (P)
+            memcpy(P + i * M * N, Pi, sizeof(double) * (size_t)(M * N));
+    }
+    free(Xi);
+    free(Pi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Megatron-style MLP block ([TP-topic] Megatron-LM, "MLP Layer Splitting":  */
+/* first linear split by columns, activation applied independently per      */
+/* shard, second linear split by rows, one sum at the end; [TP-topic]        */
+/* "Row-Wise Parallelism": the row-split input is already split by the      */
+/* preceding column-split layer).                                            */
+/*                                                                           */
+/* X [M,d], W1 [d,f], W2 [f,d].  Shard i: H_i = GeLU(X . W1_i) [M, f/n];     */
+/* P_i = H_i . W2_i with W2_i = rows [i*f/n, (i+1)*f/n) of W2;               */
+/* Y = sum_i P_i (ascending i).                                              */
+/* If mirror_h_bf16 != 0, H_i is rounded to bf16 before the second product  */
+/* (a diagnostic that separates rounding of the hidden activation from       */
+/* other differences; it is not the reference result).                       */
+/* ------------------------------------------------------------------------ */
+void orc_mlp_block(const double *X, const double *W1, const double *W2, double *Y,
+                   int64_t M, int64_t d, int64_t f, int64_t n_shards, int mirror_h_bf16)
+{
+    const int64_t fs = f / n_shards;
+    double *W1i = (double *)malloc(sizeof(double) * (size_t)(d * fs > 0 ? d * fs : 1));
+    double *Hi = (double *)malloc(sizeof(double) * (size_t)(M * fs > 0 ? M * fs : 1));
+    double *Pi = (double *)malloc(sizeof(double) * (size_t)(M * d > 0 ? M * d : 1));
+    for (int64_t t = 0; t < M * d; ++t)
+        Y[t] = 0.0;
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t k = 0; k < d; ++k)
+            for (int64_t j = 0; j < fs; ++j)
+                W1i[k * fs + j] = W1[k * f + i * fs + j];
+        orc_matmul(X, W1i, Hi, M, d, fs);
+        orc_gelu_inplace(Hi, M * fs);
+        if (mirror_h_bf16)
+            for (int64_t t = 0; t < M * fs; ++t)
+                Hi[t] = orc_bf16_to_double(orc_bf16_from_double(Hi[t]));
+        orc_matmul(Hi, W2 + i * fs * d, Pi, M, fs, d);
+        for (int64_t t = 0; t < M * d; ++t)
+            Y[t] += Pi[t];
+    }
+    free(W1i);
+    free(Hi);
+    free(Pi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The two combine steps on their own.                                       */
+/* ------------------------------------------------------------------------ */
+
+/* All-reduce as an on-device sum: Y[r,c] = sum_i P[i,r,c] over ascending i,
+ * in double, from fp32 partials laid out [n, rows, cols]. */
+void orc_shard_reduce(const float *P, double *Y, int64_t rows, int64_t cols, int64_t n_shards)
+{
+    const int64_t total = rows * cols;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < total; ++t) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < n_shards; ++i)
+            acc += (double)P[i * total + t];
+        Y[t] = acc;
+    }
+}
+
+/* All-gather as an on-device concat: n shard outputs [n][rows, G*sw] placed
+ * into Y [rows, G*n*sw] with the same column ownership as orc_column_linear. */
+void orc_shard_concat(const double *Ys, double *Y, int64_t rows, int64_t shard_cols,
+                      int64_t n_shards, int64_t col_groups)
+{
+    const int64_t sw = shard_cols / col_groups;
+    const int64_t N = shard_cols * n_shards;
+    const int64_t gw = N / col_groups;
+    for (int64_t i = 0; i < n_shards; ++i)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t b = 0; b < col_groups; ++b)
+                for (int64_t j = 0; j < sw; ++j)
+                    Y[r * N + b * gw + i * sw + j] = Ys[(i * rows + r) * shard_cols + b * sw + j];
+}

@@ -1,0 +1,309 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each test ties one oracle function to something the pages or mathematics fix:
+the glossary page's worked example, brute force in plain Python integers,
+a library routine (scipy's normal CDF, numpy's concatenate, torch's float32
+to bf16 conversion), tabulated values, and the invariant that the sharded
+result equals the unsharded one.  The last test plants mistakes in the
+oracle's inputs and checks that the pins catch them.
+"""
+import itertools
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from tensor_sharded_linear_02_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            rows.setdefault(key, []).append([float(v) for v in vals])
+    return rows
+
+
+@pytest.fixture(scope="module")
+def worked():
+    g = _read_golden("worked_example.txt")
+    X = np.array(g["X"])
+    W = np.array(g["W"])
+    return X, W, g
+
+
+# ------------------------------------------------------- worked example -----
+
+def test_worked_example_full_product(worked):
+    X, W, g = worked
+    np.testing.assert_array_equal(oracle.matmul(X, W), np.array(g["Y"]))
+
+
+def test_worked_example_column_split(worked):
+    X, W, g = worked
+    Y, Ys = oracle.column_linear(X, W, n_shards=2)
+    np.testing.assert_array_equal(Ys[0], np.array([g["column_shard"][0]]))
+    np.testing.assert_array_equal(Ys[1], np.array([g["column_shard"][1]]))
+    np.testing.assert_array_equal(Y, np.array(g["Y"]))
+    np.testing.assert_array_equal(oracle.shard_concat(Ys), np.array(g["Y"]))
+
+
+def test_worked_example_row_split(worked):
+    X, W, g = worked
+    Y, P = oracle.row_linear(X, W, n_shards=2)
+    np.testing.assert_array_equal(P[0], np.array([g["row_partial"][0]]))
+    np.testing.assert_array_equal(P[1], np.array([g["row_partial"][1]]))
+    np.testing.assert_array_equal(Y, np.array(g["Y"]))
+    np.testing.assert_array_equal(oracle.shard_reduce(P.astype(np.float32)), np.array(g["Y"]))
+
+
+def test_combine_rule_from_quiz(worked):
+    """Glossary "Check your understanding": partials covering the same output
+    coordinates are added; outputs covering different coordinates are
+    concatenated.  The row split's partials each span all of Y; the column
+    split's shard outputs are disjoint and their widths add up to Y's."""
+    X, W, _ = worked
+    _, P = oracle.row_linear(X, W, 2)
+    _, Ys = oracle.column_linear(X, W, 2)
+    assert all(p.shape == (1, 4) for p in P)
+    assert sum(y.shape[1] for y in Ys) == 4
+
+
+# ------------------------------------------------------- brute force -------
+
+def _bf_matmul(X, W):
+    M, K = len(X), len(X[0]) if X else 0
+    N = len(W[0]) if W else 0
+    return [[sum(X[i][k] * W[k][j] for k in range(K)) for j in range(N)] for i in range(M)]
+
+
+def _divisors(n):
+    return [d for d in range(1, n + 1) if n % d == 0]
+
+
+def _rand_int_matrix(rng, r, c):
+    return [[rng.randint(-9, 9) for _ in range(c)] for _ in range(r)]
+
+
+def test_brute_force_integer_shapes():
+    """Plain Python integer loops on random tiny shapes, every shard count
+    that divides the split axis: exact equality."""
+    rng = random.Random(12345)
+    for _ in range(60):
+        M, K, N = rng.randint(1, 8), rng.randint(1, 8), rng.randint(1, 8)
+        X, W = _rand_int_matrix(rng, M, K), _rand_int_matrix(rng, K, N)
+        ref = _bf_matmul(X, W)
+        np.testing.assert_array_equal(oracle.matmul(X, W), np.array(ref, dtype=np.float64))
+        for n in _divisors(N):
+            Y, Ys = oracle.column_linear(X, W, n)
+            np.testing.assert_array_equal(Y, ref)
+            w = N // n
+            for i in range(n):
+                Wi = [row[i * w:(i + 1) * w] for row in W]
+                np.testing.assert_array_equal(Ys[i], _bf_matmul(X, Wi))
+        for n in _divisors(K):
+            Y, P = oracle.row_linear(X, W, n)
+            np.testing.assert_array_equal(Y, ref)
+            ks = K // n
+            for i in range(n):
+                Xi = [row[i * ks:(i + 1) * ks] for row in X]
+                Wi = W[i * ks:(i + 1) * ks]
+                np.testing.assert_array_equal(P[i], _bf_matmul(Xi, Wi))
+
+
+def test_brute_force_head_groups():
+    """Head-group column split (G column blocks, shard i owns slice i of each
+    block): brute force on labelled columns."""
+    rng = random.Random(7)
+    for G, n, sw in [(3, 2, 1), (3, 2, 2), (3, 4, 1), (2, 2, 3)]:
+        N = G * n * sw
+        M, K = 3, 4
+        X, W = _rand_int_matrix(rng, M, K), _rand_int_matrix(rng, K, N)
+        ref = _bf_matmul(X, W)
+        Y, Ys = oracle.column_linear(X, W, n, col_groups=G)
+        np.testing.assert_array_equal(Y, ref)
+        for i in range(n):
+            cols = [b * (N // G) + i * sw + j for b in range(G) for j in range(sw)]
+            np.testing.assert_array_equal(Ys[i], [[r[c] for c in cols] for r in ref])
+        np.testing.assert_array_equal(oracle.shard_concat(Ys, col_groups=G), ref)
+
+
+def test_mlp_brute_force_with_library_gelu():
+    """MLP block on tiny shapes against plain loops whose GeLU is
+    x * scipy.special.ndtr(x) (a library normal CDF, not the oracle's erf)."""
+    rng = np.random.default_rng(3)
+    for M, d, f, n in [(3, 4, 8, 2), (2, 5, 6, 3), (4, 3, 4, 4), (1, 2, 2, 1)]:
+        X = rng.standard_normal((M, d))
+        W1 = rng.standard_normal((d, f))
+        W2 = rng.standard_normal((f, d))
+        H = [[sum(X[i, k] * W1[k, j] for k in range(d)) for j in range(f)] for i in range(M)]
+        H = [[h * float(scipy.special.ndtr(h)) for h in row] for row in H]
+        Y = [[sum(H[i][k] * W2[k, j] for k in range(f)) for j in range(d)] for i in range(M)]
+        got = oracle.mlp_block(X, W1, W2, n)
+        np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------- sharded == unsharded --------
+
+def test_sharded_equals_unsharded_float():
+    """Sharded result equals the unsharded one for every shard count
+    ([TP-topic] Implementation Considerations: same results as one device),
+    up to double reassociation in the row/MLP sums."""
+    rng = np.random.default_rng(11)
+    M, K, N = 5, 24, 24
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N))
+    ref = oracle.matmul(X, W)
+    for n in _divisors(24):
+        Y, _ = oracle.column_linear(X, W, n)
+        np.testing.assert_array_equal(Y, ref)  # same dot products, same order
+        Y, P = oracle.row_linear(X, W, n)
+        np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+    W1 = rng.standard_normal((K, 48)) * 0.2
+    W2 = rng.standard_normal((48, K)) * 0.2
+    ref = oracle.mlp_block(X, W1, W2, 1)
+    for n in _divisors(48):
+        np.testing.assert_allclose(oracle.mlp_block(X, W1, W2, n), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_equals_composed_steps():
+    """MLP block = row split of GeLU(column split) with the column output
+    never concatenated ([TP-topic] Row-Wise: the input is already split)."""
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((6, 8))
+    W1 = rng.standard_normal((8, 16))
+    W2 = rng.standard_normal((16, 8))
+    for n in (1, 2, 4, 8):
+        H, _ = oracle.column_linear(X, W1, n, act="gelu")
+        Y, _ = oracle.row_linear(H, W2, n)
+        np.testing.assert_allclose(oracle.mlp_block(X, W1, W2, n), Y, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------- GeLU ------
+
+def test_gelu_against_library_cdf():
+    x = np.concatenate([np.linspace(-12, 12, 4001), inputs.normal((5000,), 99, 3.0)])
+    ref = x * scipy.special.ndtr(x)
+    np.testing.assert_allclose(oracle.gelu(x), ref, rtol=1e-13, atol=1e-300)
+
+
+def test_gelu_textbook_values():
+    g = _read_golden("gelu_textbook.txt")
+    for x, phi in (row for key, rows in g.items() for row in [[float(key)] + r for r in rows]):
+        assert abs(oracle.gelu([x])[0] - x * phi) <= 1e-9 * max(1.0, abs(x))
+
+
+def test_gelu_special_values():
+    assert oracle.gelu([0.0])[0] == 0.0
+    x = np.linspace(-8, 8, 257)
+    # x*Phi(x) - (-x)*Phi(-x) = x*(Phi(x) + Phi(-x)) = x
+    np.testing.assert_allclose(oracle.gelu(x) - oracle.gelu(-x), x, rtol=0, atol=1e-14)
+    assert oracle.gelu([40.0])[0] == 40.0
+    assert oracle.gelu([-40.0])[0] == 0.0 or abs(oracle.gelu([-40.0])[0]) < 1e-300
+
+
+# --------------------------------------------------------------- bf16 ------
+
+def test_bf16_hand_cases():
+    f = oracle.f64_to_bf16
+    cases = [
+        (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+        (1.0 + 2.0 ** -8, 0x3F80),            # tie -> even (mantissa 0)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),        # tie -> even (mantissa 2)
+        (1.0 + 2.0 ** -8 + 2.0 ** -20, 0x3F81),  # just above the tie
+        (3.3895313892515355e38, 0x7F7F),      # largest finite bf16
+        (3.4e38, 0x7F80),                     # rounds past the largest finite
+        (2.0 ** -133, 0x0001),                # smallest subnormal
+        (2.0 ** -134, 0x0000),                # tie between 0 and 2^-133 -> even (0)
+        (3 * 2.0 ** -134, 0x0002),            # tie between 1 and 2 quanta -> even
+        (2.0 ** -126, 0x0080),                # smallest normal
+        (float("inf"), 0x7F80), (float("-inf"), 0xFF80),
+    ]
+    for x, bits in cases:
+        assert int(f(np.array([x]))[0]) == bits, (x, hex(int(f(np.array([x]))[0])), hex(bits))
+    assert np.isnan(oracle.bf16_to_f64(f(np.array([float("nan")]))))[0]
+    for bits in (0x3F80, 0xC000, 0x0001, 0x0080, 0x7F7F, 0x8001):
+        v = oracle.bf16_to_f64(np.array([bits], dtype=np.uint16))[0]
+        assert int(f(np.array([v]))[0]) == bits
+
+
+def test_bf16_against_torch_from_float32():
+    """For float32 sources (no double rounding) the oracle's RNE must agree
+    with torch's float32 -> bfloat16 conversion bit for bit."""
+    import torch
+    rng = np.random.default_rng(0)
+    bits32 = rng.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x32 = bits32.view(np.float32)
+    x32 = x32[np.isfinite(x32)]
+    ours = oracle.f64_to_bf16(x32.astype(np.float64))
+    theirs = torch.from_numpy(x32.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, theirs)
+    back = oracle.bf16_to_f64(theirs)
+    np.testing.assert_array_equal(back, torch.from_numpy(theirs.view(np.int16).copy()).view(torch.bfloat16).double().numpy())
+
+
+# ------------------------------------------------------- reduce/concat -----
+
+def test_reduce_integer_exact_and_float_vs_fsum():
+    rng = np.random.default_rng(2)
+    P = rng.integers(-1000, 1000, size=(5, 7, 9)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.shard_reduce(P), P.astype(np.int64).sum(axis=0))
+    P = rng.standard_normal((16, 3, 5)).astype(np.float32)
+    got = oracle.shard_reduce(P)
+    for r, c in itertools.product(range(3), range(5)):
+        ref = math.fsum(float(v) for v in P[:, r, c])
+        assert abs(got[r, c] - ref) <= 1e-15 * max(1.0, abs(ref))
+
+
+def test_concat_against_numpy():
+    rng = np.random.default_rng(4)
+    Ys = rng.standard_normal((4, 6, 8))
+    np.testing.assert_array_equal(oracle.shard_concat(Ys), np.concatenate(list(Ys), axis=1))
+
+
+# ----------------------------------------------- inputs (generator) --------
+
+def test_generator_reproducible_and_shaped():
+    a = inputs.bf16_normal((64, 48), inputs.stream_seed(0, 1), 0.02)
+    b = inputs.bf16_normal((64, 48), inputs.stream_seed(0, 1), 0.02)
+    np.testing.assert_array_equal(a, b)
+    v = oracle.bf16_to_f64(a)
+    assert abs(v.std() - 0.02) < 0.002 and abs(v.mean()) < 0.002
+    ints = inputs.int_uniform((16, 32), inputs.stream_seed(0, 0))
+    assert set(np.unique(ints)).issubset(set(range(-4, 5)))
+    assert len(np.unique(ints)) == 9
+    z = inputs.normal((200000,), 5)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+
+
+# ------------------------------------------- planted mistakes are caught ---
+
+def test_pins_catch_planted_mistakes(worked):
+    """Feed the oracle the mistakes a wrong implementation would make and
+    check that the worked-example pins reject each of them."""
+    X, W, g = worked
+    Y = np.array(g["Y"])
+    # transposed operand: the 2x4 W read as its 4x2 transpose's layout
+    Wt = W.T.reshape(2, 4)
+    assert not np.array_equal(oracle.matmul(X, Wt), Y)
+    # dropped shard in the row-split sum
+    _, P = oracle.row_linear(X, W, 2)
+    assert not np.array_equal(P[0], Y)
+    # wrong row-split pairing: X_0 with W_1 (an index slip)
+    assert not np.array_equal(X[:, :1] * W[1:2] + X[:, 1:] * W[0:1], Y)
+    # swapped column shards in the concat
+    _, Ys = oracle.column_linear(X, W, 2)
+    assert not np.array_equal(np.concatenate([Ys[1], Ys[0]], axis=1), Y)
+    # a sign error in GeLU's odd part would break x*Phi(x) at x=1
+    assert abs(oracle.gelu([1.0])[0] - 0.8413447461) < 1e-9
+    assert abs(0.5 * (1 - math.erf(1 / math.sqrt(2))) - 0.8413447461) > 0.1
