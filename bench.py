@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of the sharded MLP block (and the standalone shard reduce /
+concat) on B300, printing one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Default workload: the Megatron MLP block with X [2048, 1024] ~ N(0,1),
+W1 [1024, 4096] and W2 [4096, 1024] ~ N(0, 0.02), N = 2 logical shards
+(column GEMM + exact GeLU, row GEMM with the shard sum in the accumulator).
+A step is one tp_mlp_block call.  Its working set (about 40 MB) fits in the
+126 MB L2, so L2 is flushed (a 256 MB device write) before every timed step,
+outside the timed interval.  Each step is timed with CUDA events on the
+launching stream; the sum over K steps is the device time.
+
+Also reported on the same line:
+  roofline      the dominant kernel of the step (per-kernel event timing of
+                the same two launches) against the measured bf16 peak
+  reduce        the standalone shard reduce, N = 8 fp32 partials
+                [8, 4096, 8192] -> bf16 (1.14 GB per launch, larger than L2)
+  concat        the standalone head-group concat, 8 x [8192, 1536] bf16 ->
+                [8192, 12288] (Q|K|V blocks)
+  e2e           the same MLP metric through the C ABI with the input copied
+                from pinned host memory and the output copied back, per step
+  cpu_baseline  the fp64 oracle on the host cores, same workload
+  clocks        SM clock and throttle reasons sampled through NVML during the
+                timed region
+
+--impl reference times the oracle (plain fp64 host C) on a bounded sample of
+the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOADS = {
+    # name: (M tokens, d model, f intermediate, N shards, weight std)
+    "mlp_2048x1024x4096_n2": (2048, 1024, 4096, 2, 0.02),
+    "mlp_4096x4096x16384_n8": (4096, 4096, 16384, 8, 0.02),
+    "mlp_4096x8192x28672_n8": (4096, 8192, 28672, 8, 0.01),
+}
+DEFAULT_WORKLOAD = "mlp_2048x1024x4096_n2"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------- clocks ------
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons of one GPU through NVML (read
+    only) every few milliseconds while running."""
+
+    def __init__(self, torch_device, period_s: float = 0.005):
+        self.device, self.period = torch_device, period_s
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        self.error = None
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = self._handle_for(pynvml)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        except Exception as e:  # no NVML: report the gap instead of guessing
+            self.error = repr(e)
+        return self
+
+    def _handle_for(self, nv):
+        # CUDA and NVML number devices differently; match by UUID.
+        import torch
+        want = str(getattr(torch.cuda.get_device_properties(self.device), "uuid", "")).lower()
+        for i in range(nv.nvmlDeviceGetCount()):
+            h = nv.nvmlDeviceGetHandleByIndex(i)
+            u = nv.nvmlDeviceGetUUID(h)
+            u = (u.decode() if isinstance(u, bytes) else u).lower()
+            if want and want.replace("gpu-", "") in u:
+                return h
+        return nv.nvmlDeviceGetHandleByIndex(0)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append((mhz, reasons))
+            except Exception as e:
+                self.error = repr(e)
+            time.sleep(self.period)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
+                    "samples": 0, "error": self.error}
+        nv = self._nv
+        names = {
+            "gpu_idle": getattr(nv, "nvmlClocksEventReasonGpuIdle", 0x1),
+            "applications_clocks_setting": getattr(nv, "nvmlClocksEventReasonApplicationsClocksSetting", 0x2),
+            "sw_power_cap": getattr(nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
+            "hw_slowdown": getattr(nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
+            "sync_boost": getattr(nv, "nvmlClocksEventReasonSyncBoost", 0x10),
+            "sw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+            "hw_thermal_slowdown": getattr(nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+            "hw_power_brake_slowdown": getattr(nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+        }
+        seen = 0
+        for _, r in self.samples:
+            seen |= int(r)
+        reasons = sorted(k for k, bit in names.items() if seen & bit and k != "gpu_idle")
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ helpers ------
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _bf16_dev(bits, dev):
+    import torch
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _make_mlp_inputs(M, d, f, std, dev):
+    from tensor_sharded_linear_02_b300 import inputs
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(1, 0), 1.0)
+    w1 = inputs.bf16_normal((d, f), inputs.stream_seed(1, 1), std)
+    w2 = inputs.bf16_normal((f, d), inputs.stream_seed(1, 2), std)
+    return xb, w1, w2
+
+
+def cpu_oracle_mlp(xb, w1, w2, n, rows, repeats=1):
+    """Time the fp64 oracle on the first `rows` rows of the workload."""
+    import oracle
+    X = oracle.bf16_to_f64(xb[:rows])
+    W1, W2 = oracle.bf16_to_f64(w1), oracle.bf16_to_f64(w2)
+    d, f = W1.shape
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.mlp_block(X, W1, W2, n)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * d * f * 2
+    return flops, times
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------- our arm ---------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from tensor_sharded_linear_02_b300 import binding as tp
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+
+    M, d, f, n, std = WORKLOADS[args.workload]
+    xb, w1b, w2b = _make_mlp_inputs(M, d, f, std, dev)
+    X, W1, W2 = _bf16_dev(xb, dev), _bf16_dev(w1b, dev), _bf16_dev(w2b, dev)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    H = ws[: M * f * 2].view(torch.bfloat16).view(M, f)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flops_k1 = 2.0 * M * d * f
+    flops_k2 = 2.0 * M * f * d
+    flops_step = flops_k1 + flops_k2
+
+    def step():
+        tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error during warm-up")
+
+    # ---------------------------------------------------- timed region ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the timed region")
+
+    # per-kernel attribution: the same two GEMM launches with an event between
+    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev3[i][0].record(stream)
+        tp.tp_column_linear(X, W1, H, None, n_shards=n, act="gelu")
+        ev3[i][1].record(stream)
+        tp.tp_row_linear(H, W2, Y, None, n_shards=n)
+        ev3[i][2].record(stream)
+    torch.cuda.synchronize()
+    k1_ms = sum(a.elapsed_time(b) for a, b, _ in ev3) / K
+    k2_ms = sum(b.elapsed_time(c) for _, b, c in ev3) / K
+
+    # -------------------------------------------------- standalone reduce ---
+    red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
+    cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
+
+    # --------------------------------------------------------------- e2e ----
+    Xh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Yh = torch.empty(M, d, dtype=torch.bfloat16).pin_memory()
+    Ke = min(K, 500)
+    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ke)]
+    torch.cuda.synchronize()
+    for i in range(Ke):
+        eve[i][0].record(stream)
+        X.copy_(Xh, non_blocking=True)
+        step()
+        Yh.copy_(Y, non_blocking=True)
+        eve[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
+
+    # --------------------------------------------------- max over ranks -----
+    t = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev_ms, e2e_ms = float(t[0]), float(t[1])
+    ms_per_step = dev_ms / K
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    dom_ms, dom_flops, dom_name = ((k1_ms, flops_k1, "gemm column + GeLU (X.W1)")
+                                   if k1_ms >= k2_ms else
+                                   (k2_ms, flops_k2, "gemm row + shard sum (H.W2)"))
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = _profile_traffic(args.workload)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        flops_s, times = cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)
+        cpu = {"value": flops_s / min(times) / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
+               "kind": "oracle",
+               "sample": f"full workload ({M} rows), fp64 naive loops, 1 pass, "
+                         f"{min(times):.2f} s"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": "sharded MLP-block TFLOP/s on 1 B300 (% bf16 dense peak); shard-reduce HBM GB/s",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, bf16)",
+        "config": {"workload": args.workload, "M": M, "d": d, "f": f, "n_shards": n,
+                   "weight_std": std, "flops_per_step": flops_step,
+                   "l2": "flushed before every timed step (256 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "frac_of_peak": round(value / peak, 4),
+        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": peaks["source"] + " burst bf16",
+                     "kernel_ms": {"gemm_column_gelu": round(k1_ms, 5),
+                                   "gemm_row_shard_sum": round(k2_ms, 5)}},
+        "reduce": red,
+        "concat": cat,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * d * 2,
+                "ms_per_step": round(e2e_ms, 5),
+                "note": "X copied from pinned host memory, tp_mlp_block, Y copied back"},
+        "gpu_launches": 2 * K,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "wall_s_timed_loop": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _profile_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture of the current kernel build, or None when there is none."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh).get(workload)
+    except (OSError, ValueError):
+        return None
+
+
+def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
+    import torch
+    from tensor_sharded_linear_02_b300 import inputs
+    P = torch.from_numpy(inputs.f32_normal((n, rows, cols), 4242)).to(dev)
+    Y = torch.empty(rows, cols, dtype=torch.bfloat16, device=dev)
+    for _ in range(5):
+        tp.tp_shard_reduce(P, Y)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        ev[i][0].record(stream)
+        tp.tp_shard_reduce(P, Y)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    nbytes = (4 * n + 2) * rows * cols
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"reduce {n} x [{rows},{cols}] fp32 -> bf16", "value": round(gbs, 1),
+            "unit": "GB/s", "ms_per_launch": round(ms, 5), "bytes_per_launch": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"] + " copy bandwidth"},
+            "l2": "inputs (1.07 GB) larger than L2"}
+
+
+def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=3):
+    import torch
+    Ys = torch.empty(n, rows, sc, dtype=torch.bfloat16, device=dev).normal_()
+    Y = torch.empty(rows, n * sc, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        tp.tp_shard_concat_grouped(Ys, Y, col_groups=groups)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        tp.tp_shard_concat_grouped(Ys, Y, col_groups=groups)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    nbytes = 2 * n * rows * sc * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"concat {n} x [{rows},{sc}] bf16, {groups} column groups",
+            "value": round(gbs, 1), "unit": "GB/s", "ms_per_launch": round(ms, 5),
+            "bytes_per_launch": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"] + " copy bandwidth"},
+            "l2": "flushed before every timed launch"}
+
+
+# ------------------------------------------------------ reference arm ------
+
+def run_reference(args):
+    """The oracle (plain fp64 host loops) as the reference arm: each step is
+    a bounded sample of the workload (its first R rows of X)."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    M, d, f, n, std = WORKLOADS[args.workload]
+    xb, w1b, w2b = _make_mlp_inputs(M, d, f, std, None)
+    import oracle
+    W1, W2 = oracle.bf16_to_f64(w1b), oracle.bf16_to_f64(w2b)
+    # size the per-step sample so that warm-up + K steps take about
+    # args.ref_seconds of host time
+    Xc = oracle.bf16_to_f64(xb[:8])
+    t0 = time.perf_counter()
+    oracle.mlp_block(Xc, W1, W2, n)
+    per_row = (time.perf_counter() - t0) / 8
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    rows = max(1, min(M, int(budget / max(per_row, 1e-9))))
+    X = oracle.bf16_to_f64(xb[:rows])
+    for _ in range(args.warmup):
+        oracle.mlp_block(X, W1, W2, n)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.mlp_block(X, W1, W2, n)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * d * f * 2
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference",
+        "metric": "sharded MLP-block TFLOP/s on 1 B300 (% bf16 dense peak); shard-reduce HBM GB/s",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, bf16 inputs widened to f64)",
+        "config": {"workload": args.workload, "M": M, "d": d, "f": f, "n_shards": n,
+                   "weight_std": std},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _host_cores(),
+                         "kind": "oracle",
+                         "sample": f"first {rows} of {M} rows per step, fp64 naive loops"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="host-time budget of the reference arm (sets its per-step sample)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+"""Thin ctypes binding of ``libtp_b300.so`` (the C ABI in ``include/tp.h``).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the current CUDA device, reads their pointers, sizes and dtypes, and
+calls the C entry point of the same name on the current torch stream.  No
+arithmetic of the method happens here, and there is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtp_b300.so")
+
+TP_OK = 0
+TP_ERR_DEVICE_TIMEOUT = 8
+TP_F32, TP_BF16 = 0, 1
+TP_SPLIT_COLS, TP_SPLIT_ROWS = 0, 1
+TP_ACT_NONE, TP_ACT_GELU = 0, 1
+TP_MAX_SHARDS = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TPError(RuntimeError):
+    """A library call returned a status other than TP_OK."""
+
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {message}")
+        self.status = status
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+SIGNATURES = {
+    "tp_column_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int, _vp], _int),
+    "tp_column_linear_grouped": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int,
+                                  _int, _vp], _int),
+    "tp_row_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp], _int),
+    "tp_sharded_linear": ([_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int, _int, _vp],
+                          _int),
+    "tp_shard_reduce": ([_vp, _vp, _i64, _i64, _int, _int, _vp], _int),
+    "tp_shard_concat": ([_vp, _vp, _i64, _i64, _int, _int, _vp], _int),
+    "tp_shard_concat_grouped": ([_vp, _vp, _i64, _i64, _int, _int, _int, _vp], _int),
+    "tp_mlp_block_workspace_size": ([_i64, _i64, _int], ctypes.c_size_t),
+    "tp_mlp_block": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i64, _i64, _i64, _int, _int,
+                      _int, _vp], _int),
+    "tp_get_device_status": ([_vp], _int),
+    "tp_selftest_bounded_wait": ([ctypes.c_uint64, _vp], _int),
+    "tp_status_string": ([_int], ctypes.c_char_p),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load the shared library (once) and declare every entry point."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it first (python -c "
+                    f"'import __graft_entry__; __graft_entry__.build()')")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+        return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != TP_OK:
+        msg = lib().tp_status_string(status).decode()
+        raise TPError(fn, status, msg)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t == torch.bfloat16:
+        return TP_BF16
+    if t == torch.float32:
+        return TP_F32
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _act(act) -> int:
+    if act in (None, "none", TP_ACT_NONE):
+        return TP_ACT_NONE
+    if act in ("gelu", TP_ACT_GELU):
+        return TP_ACT_GELU
+    raise ValueError(f"unknown activation {act!r}")
+
+
+def _out_dtype(Y, Ys):
+    return (Y if Y is not None else Ys).dtype
+
+
+# --------------------------------------------------------------- entries ---
+
+def tp_column_linear(X, W, Y=None, Y_shards=None, n_shards=1, act=None, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_column_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(Y_shards), M, K, N, n_shards,
+                                _dtype_code(X.dtype), _dtype_code(_out_dtype(Y, Y_shards)),
+                                _act(act), _stream(stream))
+    _check("tp_column_linear", st)
+
+
+def tp_column_linear_grouped(X, W, Y=None, Y_shards=None, n_shards=1, col_groups=1, act=None,
+                             stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_column_linear_grouped(_ptr(X), _ptr(W), _ptr(Y), _ptr(Y_shards), M, K, N,
+                                        n_shards, col_groups, _dtype_code(X.dtype),
+                                        _dtype_code(_out_dtype(Y, Y_shards)), _act(act),
+                                        _stream(stream))
+    _check("tp_column_linear_grouped", st)
+
+
+def tp_row_linear(X, W, Y=None, P_out=None, n_shards=1, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    out_t = _dtype_code(Y.dtype) if Y is not None else TP_F32
+    st = lib().tp_row_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(P_out), M, K, N, n_shards,
+                             _dtype_code(X.dtype), out_t, _stream(stream))
+    _check("tp_row_linear", st)
+
+
+def tp_sharded_linear(X, W, Y, n_shards=1, split=TP_SPLIT_COLS, act=None, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_sharded_linear(_ptr(X), _ptr(W), _ptr(Y), M, K, N, n_shards, split,
+                                 _dtype_code(X.dtype), _dtype_code(Y.dtype), _act(act),
+                                 _stream(stream))
+    _check("tp_sharded_linear", st)
+
+
+def tp_shard_reduce(P, Y, stream=None):
+    n, rows, cols = P.shape
+    st = lib().tp_shard_reduce(_ptr(P), _ptr(Y), rows, cols, n, _dtype_code(Y.dtype),
+                               _stream(stream))
+    _check("tp_shard_reduce", st)
+
+
+def tp_shard_concat(Ys, Y, stream=None):
+    n, rows, sc = Ys.shape
+    st = lib().tp_shard_concat(_ptr(Ys), _ptr(Y), rows, sc, n, _dtype_code(Ys.dtype),
+                               _stream(stream))
+    _check("tp_shard_concat", st)
+
+
+def tp_shard_concat_grouped(Ys, Y, col_groups=1, stream=None):
+    n, rows, sc = Ys.shape
+    st = lib().tp_shard_concat_grouped(_ptr(Ys), _ptr(Y), rows, sc, n, col_groups,
+                                       _dtype_code(Ys.dtype), _stream(stream))
+    _check("tp_shard_concat_grouped", st)
+
+
+def tp_mlp_block_workspace_size(M, f, dtype) -> int:
+    return int(lib().tp_mlp_block_workspace_size(M, f, _dtype_code(dtype)))
+
+
+def tp_mlp_block(X, W1, W2, Y, ws, n_shards=1, stream=None):
+    M, d = X.shape
+    f = W1.shape[1]
+    st = lib().tp_mlp_block(_ptr(X), _ptr(W1), _ptr(W2), _ptr(Y), _ptr(ws),
+                            ws.numel() * ws.element_size(), M, d, f, n_shards,
+                            _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
+    _check("tp_mlp_block", st)
+
+
+def tp_get_device_status(stream=None) -> int:
+    """Synchronise and return the device status code (TP_OK or an error)."""
+    return int(lib().tp_get_device_status(_stream(stream)))
+
+
+def tp_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    _check("tp_selftest_bounded_wait", lib().tp_selftest_bounded_wait(limit_ns, _stream(stream)))
+
+
+def tp_status_string(status: int) -> str:
+    return lib().tp_status_string(status).decode()

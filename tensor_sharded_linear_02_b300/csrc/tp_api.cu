@@ -1,0 +1,590 @@
+// tp_api.cu -- host side of the C ABI declared in include/tp.h: argument
+// validation, tensor-map encoding, kernel selection and launch.  This is the
+// library's only translation unit; the kernels come in through the headers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tp.h"
+#include "gemm_tcgen05.cuh"
+#include "shard_combine.cuh"
+#include "simt_linear.cuh"
+
+namespace {
+
+using namespace tpk;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kInt32Max = 0x7FFFFFFF;
+
+// ----------------------------------------------------------------- devices --
+
+struct DeviceInfo {
+    int sm_count = 0;
+    bool ready = false;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+tp_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TP_ERR_CUDA;
+        if (cudaFuncSetAttribute(gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES) != cudaSuccess)
+            return TP_ERR_CUDA;
+        if (cudaFuncSetAttribute(gemm_cluster_sum_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_BYTES) != cudaSuccess)
+            return TP_ERR_CUDA;
+        d.ready = true;
+    }
+    *out = &d;
+    return TP_OK;
+}
+
+uint64_t wait_limit_ns() {
+    static uint64_t limit = [] {
+        const char *e = std::getenv("TP_WAIT_LIMIT_MS");
+        uint64_t ms = e ? std::strtoull(e, nullptr, 10) : 4000ull;
+        if (ms < 1) ms = 1;
+        return ms * 1000000ull;
+    }();
+    return limit;
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+               uint32_t b2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- validation --
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A pointer is required unless the buffer it names holds no bytes.
+bool present(const void *p, size_t bytes) { return p != nullptr || bytes == 0; }
+
+size_t dtype_size(tp_dtype t) { return t == TP_BF16 ? 2 : 4; }
+
+bool valid_dtype(tp_dtype t) { return t == TP_F32 || t == TP_BF16; }
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    if (!a || !b || abytes == 0 || bbytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+tp_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// -------------------------------------------------------------- launchers --
+
+struct GemmCall {
+    const void *A;  // [M, K] bf16 row-major
+    const void *B;  // [K, N] bf16 row-major
+    int64_t M, N, K;
+    int k_groups;   // 1: one accumulator over all of K; n: one output per shard
+    void *out;
+    int64_t out_group_stride;
+    bool out_f32;
+    bool gelu;
+    void *out_shards;
+    int n_shards, col_groups;
+    bool allow_split;
+};
+
+// Cluster size for outputs with too few tiles to occupy the GPU: the largest
+// power of two S <= 8 with tiles * S <= SM count and at least one k-block
+// per CTA.  1 means the persistent kernel.
+int choose_split(int tiles, int k_blocks, int sm_count) {
+    int S = 1;
+    while (S * 2 <= 8 && static_cast<int64_t>(tiles) * S * 2 <= sm_count && S * 2 <= k_blocks)
+        S *= 2;
+    return S;
+}
+
+tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
+    DeviceInfo *dev = nullptr;
+    tp_status st = device_info(&dev);
+    if (st != TP_OK) return st;
+
+    const int64_t Kg = c.K / c.k_groups;
+    CUtensorMap tmA, tmB;
+    // A viewed as [M][k_groups][Kg]; box = 128 rows x 64 k of one group.
+    if (!encode_3d(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK, 1, BM)) return TP_ERR_CUDA;
+    // B viewed as [k_groups][Kg][N]; box = 64 k-rows x 64 columns of one group.
+    if (!encode_3d(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
+        return TP_ERR_CUDA;
+
+    GemmArgs a{};
+    a.M = static_cast<int>(c.M);
+    a.N = static_cast<int>(c.N);
+    a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
+    a.k_groups = c.k_groups;
+    a.m_tiles = static_cast<int>((c.M + BM - 1) / BM);
+    a.n_tiles = static_cast<int>((c.N + BN - 1) / BN);
+    a.num_units = a.m_tiles * a.n_tiles * c.k_groups;
+    a.out = c.out;
+    a.out_group_stride = c.out_group_stride;
+    a.out_f32 = c.out_f32 ? 1 : 0;
+    a.act_gelu = c.gelu ? 1 : 0;
+    a.out_shards = c.out_shards;
+    if (c.out_shards) {
+        a.shard_gw = static_cast<int>(c.N / c.col_groups);
+        a.shard_sw = a.shard_gw / c.n_shards;
+        a.shard_nl = a.shard_sw * c.col_groups;
+    }
+    a.wait_limit_ns = wait_limit_ns();
+
+    const int tiles = a.m_tiles * a.n_tiles;
+    const int S = (c.allow_split && c.k_groups == 1) ? choose_split(tiles, a.k_blocks, dev->sm_count)
+                                                     : 1;
+    if (S > 1) {
+        a.split = S;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(tiles * S), 1, 1);
+        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, a) != cudaSuccess)
+            return TP_ERR_CUDA;
+        return launch_status();
+    }
+    a.split = 1;
+    const int grid = a.num_units < dev->sm_count ? a.num_units : dev->sm_count;
+    gemm_persistent_kernel<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, a);
+    return launch_status();
+}
+
+template <typename Tin, typename Tout>
+tp_status launch_simt_t(const void *X, const void *W, void *Y, void *Ys, const SimtArgs &a,
+                        cudaStream_t s) {
+    dim3 block(32, 8);
+    const int64_t gx = (a.N + 31) / 32;
+    int64_t gy = (a.M + 7) / 8;
+    if (gy > 65535) gy = 65535;
+    if (gx > 0x7FFFFFFF) return TP_ERR_SHAPE;
+    simt_linear_kernel<Tin, Tout><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
+                                    block, 0, s>>>(
+        static_cast<const Tin *>(X), static_cast<const Tin *>(W), static_cast<Tout *>(Y),
+        static_cast<Tout *>(Ys), a);
+    return launch_status();
+}
+
+tp_status launch_simt(const void *X, const void *W, void *Y, void *Ys, const SimtArgs &a,
+                      tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    if (in_t == TP_F32 && out_t == TP_F32) return launch_simt_t<float, float>(X, W, Y, Ys, a, s);
+    if (in_t == TP_F32 && out_t == TP_BF16)
+        return launch_simt_t<float, __nv_bfloat16>(X, W, Y, Ys, a, s);
+    if (in_t == TP_BF16 && out_t == TP_F32)
+        return launch_simt_t<__nv_bfloat16, float>(X, W, Y, Ys, a, s);
+    return launch_simt_t<__nv_bfloat16, __nv_bfloat16>(X, W, Y, Ys, a, s);
+}
+
+int reduce_grid(int64_t work_items, int sm_count) {
+    // whole waves of 256-thread blocks, 8 resident per SM, no more than needed
+    int64_t blocks = (work_items + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+template <bool BF16>
+tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_count,
+                          cudaStream_t s) {
+    if (total % 8 != 0) {
+        shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n);
+        return launch_status();
+    }
+    const int64_t nv = total / 8;
+    const int grid = reduce_grid(nv, sm_count);
+    switch (n) {
+        case 1: shard_reduce_kernel<1, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+        case 2: shard_reduce_kernel<2, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+        case 4: shard_reduce_kernel<4, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+        case 8: shard_reduce_kernel<8, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+        case 16: shard_reduce_kernel<16, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+        default: shard_reduce_kernel<0, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
+    }
+    return launch_status();
+}
+
+tp_status launch_reduce(const float *P, void *Y, int64_t total, int n, tp_dtype out_t,
+                        cudaStream_t s) {
+    DeviceInfo *dev = nullptr;
+    tp_status st = device_info(&dev);
+    if (st != TP_OK) return st;
+    return out_t == TP_BF16 ? launch_reduce_t<true>(P, Y, total, n, dev->sm_count, s)
+                            : launch_reduce_t<false>(P, Y, total, n, dev->sm_count, s);
+}
+
+// ------------------------------------------------------- shared validation --
+
+tp_status check_shards(int n_shards) {
+    return (n_shards >= 1 && n_shards <= TP_MAX_SHARDS) ? TP_OK : TP_ERR_DIVISIBILITY;
+}
+
+tp_status check_sizes(int64_t M, int64_t K, int64_t N) {
+    if (M < 0 || K < 0 || N < 0) return TP_ERR_SHAPE;
+    if (M > kInt32Max || K > kInt32Max || N > kInt32Max) return TP_ERR_SHAPE;
+    return TP_OK;
+}
+
+tp_status column_impl(const void *X, const void *W, void *Y, void *Ys, int64_t M, int64_t K,
+                      int64_t N, int n, int G, tp_dtype in_t, tp_dtype out_t, tp_act act,
+                      cudaStream_t s) {
+    tp_status st = check_sizes(M, K, N);
+    if (st != TP_OK) return st;
+    if (!valid_dtype(in_t) || !valid_dtype(out_t) || (act != TP_ACT_NONE && act != TP_ACT_GELU))
+        return TP_ERR_DTYPE;
+    const size_t it = dtype_size(in_t), ot = dtype_size(out_t);
+    const size_t xb = M * K * it, wb = K * N * it, yb = M * N * ot;
+    if (!present(X, xb) || !present(W, wb) || (!Y && !Ys && yb > 0)) return TP_ERR_NULL;
+    if ((st = check_shards(n)) != TP_OK) return st;
+    if (G < 1 || N % G != 0 || (N / G) % n != 0) return TP_ERR_DIVISIBILITY;
+    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W, wb) || overlaps(Ys, yb, X, xb) ||
+        overlaps(Ys, yb, W, wb) || overlaps(Y, yb, Ys, yb))
+        return TP_ERR_ALIAS;
+    const int64_t sw = N / G / n;
+    if (in_t == TP_BF16) {
+        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(Ys, 16))
+            return TP_ERR_ALIGNMENT;
+        if (K % 8 != 0 || N % 8 != 0 || (Ys && sw % 8 != 0)) return TP_ERR_ALIGNMENT;
+    } else {
+        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(Ys, ot))
+            return TP_ERR_ALIGNMENT;
+    }
+    if (M == 0 || N == 0) return TP_OK;
+    if (K == 0) {  // empty contraction: every output is act(0) = 0
+        if (Y && cudaMemsetAsync(Y, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
+        if (Ys && cudaMemsetAsync(Ys, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
+        return TP_OK;
+    }
+    if (in_t == TP_BF16) {
+        GemmCall c{};
+        c.A = X; c.B = W; c.M = M; c.N = N; c.K = K;
+        c.k_groups = 1;
+        c.out = Y; c.out_group_stride = 0; c.out_f32 = (out_t == TP_F32);
+        c.gelu = (act == TP_ACT_GELU);
+        c.out_shards = Ys; c.n_shards = n; c.col_groups = G;
+        c.allow_split = true;
+        return launch_gemm(c, s);
+    }
+    SimtArgs a{};
+    a.M = M; a.K = K; a.N = N; a.k_shards = 1; a.act_gelu = (act == TP_ACT_GELU);
+    a.partials = nullptr;
+    a.shard_gw = N / G; a.shard_sw = sw; a.shard_nl = sw * G;
+    return launch_simt(X, W, Y, Ys, a, in_t, out_t, s);
+}
+
+}  // namespace
+
+// =================================================================== C ABI ==
+
+extern "C" {
+
+const char *tp_status_string(tp_status st) {
+    switch (st) {
+        case TP_OK: return "TP_OK";
+        case TP_ERR_NULL: return "TP_ERR_NULL: a required pointer is NULL";
+        case TP_ERR_SHAPE: return "TP_ERR_SHAPE: invalid or inconsistent sizes";
+        case TP_ERR_DIVISIBILITY: return "TP_ERR_DIVISIBILITY: split axis not divisible, or shard count out of range";
+        case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT: pointer or row pitch misaligned";
+        case TP_ERR_DTYPE: return "TP_ERR_DTYPE: unsupported dtype or activation";
+        case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace missing or too small";
+        case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA call failed";
+        case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+        case TP_ERR_ALIAS: return "TP_ERR_ALIAS: an output overlaps an input";
+    }
+    return "TP_ERR_UNKNOWN";
+}
+
+tp_status tp_column_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
+                           int64_t K, int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                           tp_act act, cudaStream_t s) {
+    return column_impl(X, W, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
+}
+
+tp_status tp_column_linear_grouped(const void *X, const void *W, void *Y, void *Y_shards,
+                                   int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                   int col_groups, tp_dtype in_t, tp_dtype out_t, tp_act act,
+                                   cudaStream_t s) {
+    return column_impl(X, W, Y, Y_shards, M, K, Nout, n_shards, col_groups, in_t, out_t, act, s);
+}
+
+tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int64_t M, int64_t K,
+                        int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                        cudaStream_t s) {
+    tp_status st = check_sizes(M, K, Nout);
+    if (st != TP_OK) return st;
+    if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    const size_t it = dtype_size(in_t), ot = dtype_size(out_t);
+    const size_t xb = M * K * it, wb = K * Nout * it, yb = M * Nout * ot;
+    const size_t pb = static_cast<size_t>(n_shards) * M * Nout * 4;
+    if (!present(X, xb) || !present(W, wb) || (!Y && !P_out && yb > 0)) return TP_ERR_NULL;
+    if (K % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W, wb) || overlaps(P_out, pb, X, xb) ||
+        overlaps(P_out, pb, W, wb) || overlaps(Y, yb, P_out, pb))
+        return TP_ERR_ALIAS;
+    const int64_t Kg = K / n_shards;
+    if (in_t == TP_BF16) {
+        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(P_out, 16))
+            return TP_ERR_ALIGNMENT;
+        if (K % 8 != 0 || Nout % 8 != 0 || (P_out && Kg % 8 != 0)) return TP_ERR_ALIGNMENT;
+    } else {
+        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(P_out, 4))
+            return TP_ERR_ALIGNMENT;
+    }
+    if (P_out && Y && (!aligned(P_out, 16) || !aligned(Y, 16))) return TP_ERR_ALIGNMENT;
+    if (M == 0 || Nout == 0) return TP_OK;
+    if (K == 0) {
+        if (Y && cudaMemsetAsync(Y, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
+        if (P_out && cudaMemsetAsync(P_out, 0, pb, s) != cudaSuccess) return TP_ERR_CUDA;
+        return TP_OK;
+    }
+    if (in_t == TP_BF16) {
+        GemmCall c{};
+        c.A = X; c.B = W; c.M = M; c.N = Nout; c.K = K;
+        c.out_f32 = false; c.gelu = false; c.out_shards = nullptr; c.n_shards = n_shards;
+        c.col_groups = 1;
+        if (P_out) {
+            // one fp32 partial per shard: k-group g = shard g's rows of W
+            c.k_groups = n_shards;
+            c.out = P_out;
+            c.out_group_stride = M * Nout;
+            c.out_f32 = true;
+            c.allow_split = false;
+            if ((st = launch_gemm(c, s)) != TP_OK) return st;
+            return Y ? launch_reduce(P_out, Y, M * Nout, n_shards, out_t, s) : TP_OK;
+        }
+        // fused: the K loop walks the shards in ascending order into one
+        // fp32 accumulator (or shard groups summed through the cluster)
+        c.k_groups = 1;
+        c.out = Y;
+        c.out_group_stride = 0;
+        c.out_f32 = (out_t == TP_F32);
+        c.allow_split = true;
+        return launch_gemm(c, s);
+    }
+    SimtArgs a{};
+    a.M = M; a.K = K; a.N = Nout; a.k_shards = n_shards; a.act_gelu = 0;
+    a.partials = P_out;
+    a.shard_gw = Nout; a.shard_sw = Nout; a.shard_nl = Nout;
+    return launch_simt(X, W, Y, nullptr, a, in_t, out_t, s);
+}
+
+tp_status tp_sharded_linear(const void *X, const void *W, void *Y, int64_t M, int64_t K,
+                            int64_t Nout, int n_shards, tp_split split, tp_dtype in_t,
+                            tp_dtype out_t, tp_act act, cudaStream_t s) {
+    if (split == TP_SPLIT_COLS)
+        return tp_column_linear(X, W, Y, nullptr, M, K, Nout, n_shards, in_t, out_t, act, s);
+    if (split == TP_SPLIT_ROWS) {
+        if (act != TP_ACT_NONE) return TP_ERR_DTYPE;
+        return tp_row_linear(X, W, Y, nullptr, M, K, Nout, n_shards, in_t, out_t, s);
+    }
+    return TP_ERR_SHAPE;
+}
+
+tp_status tp_shard_reduce(const float *P, void *Y, int64_t rows, int64_t cols, int n_shards,
+                          tp_dtype out_t, cudaStream_t s) {
+    if (rows < 0 || cols < 0) return TP_ERR_SHAPE;
+    if (!valid_dtype(out_t)) return TP_ERR_DTYPE;
+    const int64_t total = rows * cols;
+    if (!present(P, total) || !present(Y, total)) return TP_ERR_NULL;
+    tp_status st = check_shards(n_shards);
+    if (st != TP_OK) return st;
+    if (!aligned(P, 16) || !aligned(Y, 16)) return TP_ERR_ALIGNMENT;
+    if (overlaps(Y, total * dtype_size(out_t), P, static_cast<size_t>(n_shards) * total * 4))
+        return TP_ERR_ALIAS;
+    if (total == 0) return TP_OK;
+    return launch_reduce(P, Y, total, n_shards, out_t, s);
+}
+
+tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t shard_cols,
+                                  int n_shards, int col_groups, tp_dtype t, cudaStream_t s) {
+    if (rows < 0 || shard_cols < 0) return TP_ERR_SHAPE;
+    if (!present(Ys, rows * shard_cols) || !present(Y, rows * shard_cols)) return TP_ERR_NULL;
+    if (!valid_dtype(t)) return TP_ERR_DTYPE;
+    tp_status st = check_shards(n_shards);
+    if (st != TP_OK) return st;
+    if (col_groups < 1 || shard_cols % col_groups != 0) return TP_ERR_DIVISIBILITY;
+    const int64_t es = static_cast<int64_t>(dtype_size(t));
+    const int64_t vec = 16 / es;
+    const int64_t sw = shard_cols / col_groups;
+    if (!aligned(Ys, 16) || !aligned(Y, 16) || sw % vec != 0) return TP_ERR_ALIGNMENT;
+    const int64_t bytes = rows * shard_cols * n_shards * es;
+    if (overlaps(Y, bytes, Ys, bytes)) return TP_ERR_ALIAS;
+    const int64_t ncv = shard_cols * n_shards / vec;  // output vectors per row
+    if (ncv > kInt32Max || rows > kInt32Max) return TP_ERR_SHAPE;
+    if (rows == 0 || ncv == 0) return TP_OK;
+    const uint32_t swv = static_cast<uint32_t>(sw / vec);
+    const uint32_t gwv = swv * static_cast<uint32_t>(n_shards);
+    const uint32_t nlv = swv * static_cast<uint32_t>(col_groups);
+    const unsigned gx = static_cast<unsigned>((ncv + 255) / 256);
+    const unsigned gy = static_cast<unsigned>(rows < 65535 ? rows : 65535);
+    shard_concat_kernel<<<dim3(gx, gy), 256, 0, s>>>(
+        static_cast<const uint4 *>(Ys), static_cast<uint4 *>(Y), rows,
+        static_cast<uint32_t>(ncv), make_fastdiv(gwv), make_fastdiv(swv), nlv);
+    return launch_status();
+}
+
+tp_status tp_shard_concat(const void *Ys, void *Y, int64_t rows, int64_t shard_cols,
+                          int n_shards, tp_dtype t, cudaStream_t s) {
+    return tp_shard_concat_grouped(Ys, Y, rows, shard_cols, n_shards, 1, t, s);
+}
+
+size_t tp_mlp_block_workspace_size(int64_t M, int64_t f, tp_dtype t) {
+    if (M < 0 || f < 0 || !valid_dtype(t)) return 0;
+    const size_t b = static_cast<size_t>(M) * static_cast<size_t>(f) * dtype_size(t);
+    return (b + 255) & ~static_cast<size_t>(255);
+}
+
+tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, void *ws,
+                       size_t ws_bytes, int64_t M, int64_t d, int64_t f, int n_shards,
+                       tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    tp_status st = check_sizes(M, d, f);
+    if (st != TP_OK) return st;
+    if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    const size_t it = dtype_size(in_t), ot = dtype_size(out_t);
+    const size_t xb = M * d * it, w1b = d * f * it, w2b = f * d * it, yb = M * d * ot;
+    const size_t hb = M * f * it;
+    if (!present(X, xb) || !present(W1, w1b) || !present(W2, w2b) || !present(Y, yb))
+        return TP_ERR_NULL;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    if (f % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    const size_t need = tp_mlp_block_workspace_size(M, f, in_t);
+    if (need > 0 && (!ws || ws_bytes < need)) return TP_ERR_WORKSPACE;
+    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W1, w1b) || overlaps(Y, yb, W2, w2b) ||
+        overlaps(Y, yb, ws, hb) || overlaps(ws, hb, X, xb) || overlaps(ws, hb, W1, w1b) ||
+        overlaps(ws, hb, W2, w2b))
+        return TP_ERR_ALIAS;
+    if (in_t == TP_BF16) {
+        if (!aligned(X, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(Y, 16) ||
+            !aligned(ws, 16))
+            return TP_ERR_ALIGNMENT;
+        if (d % 8 != 0 || f % 8 != 0) return TP_ERR_ALIGNMENT;
+    } else {
+        if (!aligned(X, 4) || !aligned(W1, 4) || !aligned(W2, 4) || !aligned(Y, ot) ||
+            !aligned(ws, 4))
+            return TP_ERR_ALIGNMENT;
+    }
+    if (M == 0 || d == 0) return TP_OK;
+    if (f == 0) return cudaMemsetAsync(Y, 0, yb, s) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+
+    if (in_t == TP_BF16) {
+        // step 1: H = GeLU(X . W1), column-parallel, H_i = column block i of H
+        GemmCall c1{};
+        c1.A = X; c1.B = W1; c1.M = M; c1.N = f; c1.K = d;
+        c1.k_groups = 1; c1.out = ws; c1.out_group_stride = 0; c1.out_f32 = false;
+        c1.gelu = true; c1.out_shards = nullptr; c1.n_shards = n_shards; c1.col_groups = 1;
+        c1.allow_split = true;
+        if ((st = launch_gemm(c1, s)) != TP_OK) return st;
+        // step 2: Y = sum_i H_i . W2_i, shard partials added in the accumulator
+        GemmCall c2{};
+        c2.A = ws; c2.B = W2; c2.M = M; c2.N = d; c2.K = f;
+        c2.k_groups = 1; c2.out = Y; c2.out_group_stride = 0; c2.out_f32 = (out_t == TP_F32);
+        c2.gelu = false; c2.out_shards = nullptr; c2.n_shards = n_shards; c2.col_groups = 1;
+        c2.allow_split = true;
+        return launch_gemm(c2, s);
+    }
+    SimtArgs a1{};
+    a1.M = M; a1.K = d; a1.N = f; a1.k_shards = 1; a1.act_gelu = 1; a1.partials = nullptr;
+    a1.shard_gw = f; a1.shard_sw = f; a1.shard_nl = f;
+    if ((st = launch_simt(X, W1, ws, nullptr, a1, TP_F32, TP_F32, s)) != TP_OK) return st;
+    SimtArgs a2{};
+    a2.M = M; a2.K = f; a2.N = d; a2.k_shards = n_shards; a2.act_gelu = 0; a2.partials = nullptr;
+    a2.shard_gw = d; a2.shard_sw = d; a2.shard_nl = d;
+    return launch_simt(ws, W2, Y, nullptr, a2, TP_F32, out_t, s);
+}
+
+tp_status tp_get_device_status(cudaStream_t s) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TP_ERR_CUDA;
+    unsigned int word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return TP_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return TP_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_timeout_site, &zero, sizeof(zero)) != cudaSuccess) return TP_ERR_CUDA;
+        return TP_ERR_DEVICE_TIMEOUT;
+    }
+    return TP_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------- bounded-wait test --
+
+namespace tpk {
+// One CTA waits on a barrier that expects one arrival nobody makes.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_wait_bounded(smem_u32(&bar), 0, limit_ns, &abort_flag, SITE_SELFTEST);
+    }
+    __syncthreads();
+}
+}  // namespace tpk
+
+extern "C" tp_status tp_selftest_bounded_wait(uint64_t limit_ns, cudaStream_t s) {
+    if (limit_ns < 1000ull) limit_ns = 1000ull;
+    if (limit_ns > 5000000000ull) limit_ns = 5000000000ull;
+    tpk::selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}

@@ -1,0 +1,64 @@
+"""Shared test helpers: moving generator output to the device and back, and
+the accuracy bar for bf16 results.
+
+Accuracy bar (bf16 inputs, fp32 accumulation, compared with the fp64
+oracle on the same input bytes):
+    relative Frobenius error  ||got - ref||_F / ||ref||_F  <= 5e-3
+    max |got - ref|                                         <= 2e-2 * RMS(ref)
+Integer-valued fp32 inputs must match exactly.
+"""
+import numpy as np
+
+import oracle
+
+REL_FRO_TOL = 5e-3
+MAX_ERR_RMS_TOL = 2e-2
+
+
+def to_dev_bf16(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_dev_f32(a, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def bf16_dev_to_f64(t):
+    import torch
+    return oracle.bf16_to_f64(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def dev_to_f64(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return bf16_dev_to_f64(t)
+    return t.detach().cpu().double().numpy()
+
+
+def dev_bits(t):
+    """Raw bit patterns of a device tensor (for bit-exact comparisons)."""
+    import torch
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().copy()
+    return t.view(torch.int32).numpy().copy()
+
+
+def errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / nref if nref > 0 else np.linalg.norm(got - ref)
+    rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
+    mx = np.max(np.abs(got - ref)) if ref.size else 0.0
+    return rel, mx, rms
+
+
+def assert_bf16_parity(got, ref, what=""):
+    rel, mx, rms = errors(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert rel <= REL_FRO_TOL, f"{what}: relative Frobenius error {rel:.3e} > {REL_FRO_TOL}"
+    assert mx <= MAX_ERR_RMS_TOL * rms, f"{what}: max |err| {mx:.3e} > {MAX_ERR_RMS_TOL} * RMS {rms:.3e}"
+    return rel, mx, rms

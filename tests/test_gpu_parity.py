@@ -1,0 +1,382 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64
+oracle on the same seeded input bytes.  Sizes span several tiles with
+ragged tails in every dimension and exercise each kernel path (persistent
+tcgen05 GEMM with and without wrap-around, the cluster split with the
+distributed-shared-memory sum, per-shard partial outputs, the CUDA-core fp32
+path, the vector and scalar reduce, plain and head-group concat)."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (assert_bf16_parity, bf16_dev_to_f64, dev_bits, dev_to_f64, to_dev_bf16,
+                     to_dev_f32)
+from tensor_sharded_linear_02_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from tensor_sharded_linear_02_b300 import binding
+    binding.lib()
+    return binding
+
+
+def _bf16_inputs(M, K, N, seed, xstd=1.0, wstd=0.02):
+    xb = inputs.bf16_normal((M, K), inputs.stream_seed(seed, 0), xstd)
+    wb = inputs.bf16_normal((K, N), inputs.stream_seed(seed, 1), wstd)
+    return xb, wb
+
+
+def _status_ok(tp):
+    assert tp.tp_get_device_status() == tp.TP_OK
+
+
+# ----------------------------------------------------------- fp32 exact -----
+
+def test_worked_example_fp32(tp, cuda_device):
+    """Glossary worked example on the device: X=[1,2], W rows [3,4,5,6] and
+    [7,8,9,10] give [17,20,23,26]; halves [17,20]|[23,26]; row partials."""
+    import torch
+    X = to_dev_f32([[1, 2]], cuda_device)
+    W = to_dev_f32([[3, 4, 5, 6], [7, 8, 9, 10]], cuda_device)
+    Y = torch.empty(1, 4, device=cuda_device)
+    Ys = torch.empty(2, 1, 2, device=cuda_device)
+    tp.tp_column_linear(X, W, Y, Ys, n_shards=2)
+    P = torch.empty(2, 1, 4, device=cuda_device)
+    Yr = torch.empty(1, 4, device=cuda_device)
+    tp.tp_row_linear(X, W, Yr, P, n_shards=2)
+    _status_ok(tp)
+    assert Y.cpu().tolist() == [[17, 20, 23, 26]]
+    assert Ys.cpu().tolist() == [[[17, 20]], [[23, 26]]]
+    assert P.cpu().tolist() == [[[3, 4, 5, 6]], [[14, 16, 18, 20]]]
+    assert Yr.cpu().tolist() == [[17, 20, 23, 26]]
+
+
+def test_tiny_integer_config_fp32(tp, cuda_device):
+    """X [16,32], W [32,64], integers uniform in [-4,4] from seed 0, two
+    shards: the column concat and the row sum both equal X.W exactly."""
+    import torch
+    X = inputs.int_uniform((16, 32), inputs.stream_seed(0, 0))
+    W = inputs.int_uniform((32, 64), inputs.stream_seed(0, 1))
+    ref = oracle.matmul(X, W)
+    ref_c, ref_s = oracle.column_linear(X, W, 2)
+    ref_r, ref_p = oracle.row_linear(X, W, 2)
+    Xd, Wd = to_dev_f32(X, cuda_device), to_dev_f32(W, cuda_device)
+    Y = torch.empty(16, 64, device=cuda_device)
+    Ys = torch.empty(2, 16, 32, device=cuda_device)
+    tp.tp_column_linear(Xd, Wd, Y, Ys, n_shards=2)
+    Yr = torch.empty(16, 64, device=cuda_device)
+    P = torch.empty(2, 16, 64, device=cuda_device)
+    tp.tp_row_linear(Xd, Wd, Yr, P, n_shards=2)
+    Yf = torch.empty(16, 64, device=cuda_device)
+    tp.tp_row_linear(Xd, Wd, Yf, None, n_shards=2)
+    Yc = torch.empty(16, 64, device=cuda_device)
+    tp.tp_shard_concat(Ys, Yc)
+    Yred = torch.empty(16, 64, device=cuda_device)
+    tp.tp_shard_reduce(P, Yred)
+    _status_ok(tp)
+    for got in (Y, Yr, Yf, Yc, Yred):
+        np.testing.assert_array_equal(dev_to_f64(got), ref)
+    np.testing.assert_array_equal(dev_to_f64(Ys), ref_s)
+    np.testing.assert_array_equal(dev_to_f64(P), ref_p)
+    np.testing.assert_array_equal(ref_c, ref)
+    np.testing.assert_array_equal(ref_r, ref)
+
+
+@pytest.mark.parametrize("M,K,N,n", [(7, 5, 9, 3), (33, 12, 20, 4), (1, 1, 1, 1)])
+def test_fp32_ragged_integer(tp, cuda_device, M, K, N, n):
+    import torch
+    X = inputs.int_uniform((M, K), inputs.stream_seed(5, 0))
+    W = inputs.int_uniform((K, N), inputs.stream_seed(5, 1))
+    ref = oracle.matmul(X, W)
+    Xd, Wd = to_dev_f32(X, cuda_device), to_dev_f32(W, cuda_device)
+    if N % n == 0:
+        Y = torch.empty(M, N, device=cuda_device)
+        tp.tp_column_linear(Xd, Wd, Y, None, n_shards=n)
+        np.testing.assert_array_equal(dev_to_f64(Y), ref)
+    if K % n == 0:
+        Y = torch.empty(M, N, device=cuda_device)
+        tp.tp_row_linear(Xd, Wd, Y, None, n_shards=n)
+        np.testing.assert_array_equal(dev_to_f64(Y), ref)
+    _status_ok(tp)
+
+
+def test_fp32_mlp_block(tp, cuda_device):
+    """fp32 MLP block on the CUDA-core path, against the oracle."""
+    import torch
+    M, d, f, n = 24, 16, 32, 4
+    X = inputs.f32_normal((M, d), 41)
+    W1 = inputs.f32_normal((d, f), 42, 0.2)
+    W2 = inputs.f32_normal((f, d), 43, 0.2)
+    Y = torch.empty(M, d, device=cuda_device)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.float32), dtype=torch.uint8,
+                     device=cuda_device)
+    tp.tp_mlp_block(to_dev_f32(X, cuda_device), to_dev_f32(W1, cuda_device),
+                    to_dev_f32(W2, cuda_device), Y, ws, n_shards=n)
+    _status_ok(tp)
+    np.testing.assert_allclose(dev_to_f64(Y), oracle.mlp_block(X, W1, W2, n), rtol=1e-5,
+                               atol=1e-5)
+
+
+# ------------------------------------------------------ bf16 column split ---
+
+COLUMN_CASES = [
+    # M, K, N, n, act      path exercised
+    (300, 328, 640, 2, None),     # cluster split, ragged M, K and N tails
+    (300, 328, 640, 2, "gelu"),
+    (2304, 136, 2080, 4, "gelu"),  # persistent, 162 tiles > SM count (TMEM ring wraps)
+    (1280, 200, 2048, 8, None),    # persistent, exactly one tile per CTA or less
+    (1, 64, 256, 1, None),         # one row
+    (129, 8, 8, 1, "gelu"),        # K one vector, N one vector
+]
+
+
+@pytest.mark.parametrize("M,K,N,n,act", COLUMN_CASES)
+def test_column_linear_bf16(tp, cuda_device, M, K, N, n, act):
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=M + K + N)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Ys = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_column_linear(X, W, Y, Ys, n_shards=n, act=act)
+    Y1 = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_column_linear(X, W, Y1, None, n_shards=1, act=act)
+    Yf = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+    tp.tp_column_linear(X, W, Yf, None, n_shards=n, act=act)
+    _status_ok(tp)
+    ref, ref_s = oracle.column_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), n, act=act)
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "column Y")
+    assert_bf16_parity(dev_to_f64(Yf), ref, "column Y fp32 out")
+    # concat fused in the store == the shard outputs, bit for bit
+    np.testing.assert_array_equal(dev_bits(Ys), dev_bits(Y).reshape(M, n, N // n).transpose(1, 0, 2))
+    # sharded == unsharded launch, bit for bit
+    np.testing.assert_array_equal(dev_bits(Y), dev_bits(Y1))
+    # fp32 output rounds to the bf16 output
+    np.testing.assert_array_equal(dev_bits(Yf.to(torch.bfloat16)), dev_bits(Y))
+
+
+@pytest.mark.parametrize("M,K,G,n,sw", [(256, 128, 3, 4, 64), (130, 64, 3, 2, 8), (64, 32, 2, 8, 16)])
+def test_column_linear_head_groups(tp, cuda_device, M, K, G, n, sw):
+    """Head-group split: shard i owns slice i of each of the G column blocks."""
+    import torch
+    N = G * n * sw
+    xb, wb = _bf16_inputs(M, K, N, seed=7 * N)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Ys = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_column_linear_grouped(X, W, Y, Ys, n_shards=n, col_groups=G)
+    Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_shard_concat_grouped(Ys, Yc, col_groups=G)
+    _status_ok(tp)
+    ref, ref_s = oracle.column_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), n,
+                                      col_groups=G)
+    assert_bf16_parity(bf16_dev_to_f64(Ys), ref_s, "grouped shard outputs")
+    np.testing.assert_array_equal(dev_bits(Yc), dev_bits(Y))
+    np.testing.assert_array_equal(bf16_dev_to_f64(Ys), oracle.bf16_to_f64(
+        dev_bits(Y).view(np.uint16)).reshape(M, G, n, sw).transpose(2, 0, 1, 3).reshape(n, M, G * sw))
+
+
+# --------------------------------------------------------- bf16 row split ---
+
+ROW_CASES = [
+    (1280, 512, 2048, 4),   # persistent (80 tiles): shards walked in one accumulator
+    (256, 1024, 512, 2),    # 4 tiles: cluster of 8, shard groups summed through DSMEM
+    (300, 384, 264, 3),     # ragged, cluster split not aligned to shards
+    (8, 64, 8, 8),          # shard depth 8 (< one k-block)
+]
+
+
+@pytest.mark.parametrize("M,K,N,n", ROW_CASES)
+def test_row_linear_bf16_fused(tp, cuda_device, M, K, N, n):
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=3 * M + K)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_row_linear(X, W, Y, None, n_shards=n)
+    _status_ok(tp)
+    ref, _ = oracle.row_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), n)
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "row fused")
+
+
+@pytest.mark.parametrize("M,K,N,n", [(300, 384, 264, 3), (256, 1024, 512, 8), (130, 64, 16, 8)])
+def test_row_linear_bf16_partials(tp, cuda_device, M, K, N, n):
+    """Per-shard fp32 partials P_i = X_i.W_i, then the standalone reduce."""
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=5 * M + N)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    P = torch.empty(n, M, N, dtype=torch.float32, device=cuda_device)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_row_linear(X, W, Y, P, n_shards=n)
+    _status_ok(tp)
+    ref, ref_p = oracle.row_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), n)
+    for i in range(n):
+        rel, mx, rms = assert_bf16_parity(dev_to_f64(P[i]), ref_p[i], f"partial {i}")
+        assert rel < 1e-5  # fp32 output of an fp32 accumulation
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "row partials + reduce")
+
+
+def test_sharded_linear_dispatch(tp, cuda_device):
+    import torch
+    M, K, N = 200, 256, 512
+    xb, wb = _bf16_inputs(M, K, N, seed=99)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Yr = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_sharded_linear(X, W, Yc, n_shards=4, split=tp.TP_SPLIT_COLS)
+    tp.tp_sharded_linear(X, W, Yr, n_shards=4, split=tp.TP_SPLIT_ROWS)
+    _status_ok(tp)
+    ref = oracle.matmul(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb))
+    assert_bf16_parity(bf16_dev_to_f64(Yc), ref, "dispatch cols")
+    assert_bf16_parity(bf16_dev_to_f64(Yr), ref, "dispatch rows")
+
+
+# ------------------------------------------------------------- MLP block ----
+
+@pytest.mark.parametrize("M,d,f,n", [(200, 256, 512, 2), (2048, 1024, 4096, 2), (384, 512, 1024, 8)])
+def test_mlp_block_bf16(tp, cuda_device, M, d, f, n):
+    """Megatron MLP block: column GEMM + GeLU, row GEMM with the shard sum
+    in the accumulator.  (2048, 1024, 4096, N=2) is the MLP-block workload
+    with X ~ N(0,1) and weights ~ N(0, 0.02)."""
+    import torch
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(1, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(1, 1), 0.02)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(1, 2), 0.02)
+    X, W1, W2 = (to_dev_bf16(b, cuda_device) for b in (xb, w1b, w2b))
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=cuda_device)
+    tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n)
+    Y2 = torch.empty_like(Y)
+    tp.tp_mlp_block(X, W1, W2, Y2, ws, n_shards=n)
+    _status_ok(tp)
+    ref = oracle.mlp_block(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(w1b),
+                           oracle.bf16_to_f64(w2b), n)
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "MLP block")
+    np.testing.assert_array_equal(dev_bits(Y), dev_bits(Y2))  # run-to-run identical
+    # the hidden activation in the workspace is GeLU(X.W1) rounded to bf16
+    H = ws[: M * f * 2].view(torch.bfloat16).view(M, f)
+    Href, _ = oracle.column_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(w1b), n, act="gelu")
+    assert_bf16_parity(bf16_dev_to_f64(H), Href, "hidden H")
+
+
+# -------------------------------------------------------- reduce / concat ---
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("rows,cols", [(64, 96), (7, 5), (1, 8)])
+def test_shard_reduce(tp, cuda_device, n, rows, cols):
+    import torch
+    P = inputs.f32_normal((n, rows, cols), 1000 + n)
+    Pd = to_dev_f32(P, cuda_device)
+    Yf = torch.empty(rows, cols, dtype=torch.float32, device=cuda_device)
+    Yb = torch.empty(rows, cols, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_shard_reduce(Pd, Yf)
+    tp.tp_shard_reduce(Pd, Yb)
+    _status_ok(tp)
+    ref = oracle.shard_reduce(P)
+    # recursive fp32 summation: |err| <= (n-1) * 2^-24 * sum_i |P_i|
+    bound = (n - 1) * 2.0 ** -24 * np.abs(P.astype(np.float64)).sum(axis=0)
+    assert np.all(np.abs(dev_to_f64(Yf) - ref) <= bound + 1e-30)
+    # the bf16 output is the round-to-nearest-even of the fp32 sum
+    np.testing.assert_array_equal(dev_bits(Yb), oracle.f64_to_bf16(dev_to_f64(Yf)).view(np.int16))
+
+
+def test_shard_reduce_integer_exact_and_specials(tp, cuda_device):
+    import torch
+    rng = np.random.default_rng(0)
+    P = rng.integers(-50, 50, size=(8, 16, 32)).astype(np.float32)
+    P[3, 0, 0] = np.nan
+    P[2, 1, 1] = np.inf
+    P[5, 2, 2] = -np.inf
+    Pd = to_dev_f32(P, cuda_device)
+    Y = torch.empty(16, 32, dtype=torch.float32, device=cuda_device)
+    tp.tp_shard_reduce(Pd, Y)
+    _status_ok(tp)
+    got = dev_to_f64(Y)
+    ref = oracle.shard_reduce(P)
+    assert np.isnan(got[0, 0]) and got[1, 1] == np.inf and got[2, 2] == -np.inf
+    mask = np.isfinite(ref)
+    np.testing.assert_array_equal(got[mask], ref[mask])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("n,rows,sc", [(8, 100, 64), (2, 16, 32), (3, 1, 8)])
+def test_shard_concat(tp, cuda_device, dtype, n, rows, sc):
+    import torch
+    Ys = inputs.f32_normal((n, rows, sc), 500 + n)
+    if dtype == "bf16":
+        bits = oracle.f64_to_bf16(Ys)
+        Ysd = to_dev_bf16(bits, cuda_device)
+        Y = torch.empty(rows, n * sc, dtype=torch.bfloat16, device=cuda_device)
+        src = oracle.bf16_to_f64(bits)
+    else:
+        Ysd = to_dev_f32(Ys, cuda_device)
+        Y = torch.empty(rows, n * sc, dtype=torch.float32, device=cuda_device)
+        src = Ys.astype(np.float64)
+    tp.tp_shard_concat(Ysd, Y)
+    _status_ok(tp)
+    np.testing.assert_array_equal(dev_to_f64(Y), oracle.shard_concat(src))
+
+
+# ------------------------------------------------------- failure handling ---
+
+def test_bounded_wait_reports_timeout(tp, cuda_device):
+    """A wait on a barrier nobody arrives on gives up after its limit and the
+    host reads TP_ERR_DEVICE_TIMEOUT; the context stays usable."""
+    import torch
+    assert tp.tp_get_device_status() == tp.TP_OK
+    tp.tp_selftest_bounded_wait(20_000_000)  # 20 ms
+    assert tp.tp_get_device_status() == tp.TP_ERR_DEVICE_TIMEOUT
+    assert tp.tp_get_device_status() == tp.TP_OK  # cleared by the read
+    P = torch.ones(2, 8, 8, device=cuda_device)
+    Y = torch.empty(8, 8, device=cuda_device)
+    tp.tp_shard_reduce(P, Y)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    assert float(Y.sum()) == 128.0
+
+
+def test_validation_errors_on_device(tp, cuda_device):
+    import torch
+    X = torch.zeros(16, 32, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.zeros(32, 64, dtype=torch.bfloat16, device=cuda_device)
+    Y = torch.zeros(16, 64, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_column_linear(X, W, Y, None, n_shards=3)
+    assert e.value.status == 3
+    big = torch.zeros(16 * 32 + 8, dtype=torch.bfloat16, device=cuda_device)
+    Xmis = big[1:1 + 16 * 32].view(16, 32)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_column_linear(Xmis, W, Y, None, n_shards=2)
+    assert e.value.status == 4
+    buf = torch.zeros(16 * 32 + 16 * 64, dtype=torch.bfloat16, device=cuda_device)
+    Xa = buf[:16 * 32].view(16, 32)
+    Ya = buf[256:256 + 16 * 64].view(16, 64)  # overlaps Xa
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_column_linear(Xa, W, Ya, None, n_shards=2)
+    assert e.value.status == 9  # output aliases an input
+    ws = torch.empty(16, dtype=torch.uint8, device=cuda_device)
+    W2 = torch.zeros(64, 32, dtype=torch.bfloat16, device=cuda_device)
+    Y2 = torch.zeros(16, 32, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_mlp_block(X, W, W2, Y2, ws, n_shards=2)
+    assert e.value.status == 6
+    assert tp.tp_get_device_status() == tp.TP_OK
+
+
+def test_empty_inputs(tp, cuda_device):
+    import torch
+    X = torch.zeros(0, 32, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.randn(32, 64, device=cuda_device).to(torch.bfloat16)
+    Y = torch.zeros(0, 64, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_column_linear(X, W, Y, None, n_shards=2)
+    tp.tp_row_linear(X, W, Y, None, n_shards=2)
+    # K = 0: the empty contraction gives zeros (and GeLU(0) = 0)
+    X0 = torch.zeros(8, 0, dtype=torch.bfloat16, device=cuda_device)
+    W0 = torch.zeros(0, 16, dtype=torch.bfloat16, device=cuda_device)
+    Y0 = torch.full((8, 16), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_column_linear(X0, W0, Y0, None, n_shards=2, act="gelu")
+    P = torch.zeros(4, 0, 8, device=cuda_device)
+    R = torch.zeros(0, 8, device=cuda_device)
+    tp.tp_shard_reduce(P, R)
+    _status_ok(tp)
+    assert float(Y0.float().abs().sum()) == 0.0
