@@ -263,13 +263,15 @@ def run_ours(args):
     k2_ms = sum(b.elapsed_time(c) for _, b, c in ev3) / K
 
     # -------------------------------------------------- standalone reduce ---
-    red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
-    cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
+    red = cat = None
+    if not args.skip_extras:
+        red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
+        cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
 
     # --------------------------------------------------------------- e2e ----
     Xh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
     Yh = torch.empty(M, d, dtype=torch.bfloat16).pin_memory()
-    Ke = min(K, 500)
+    Ke = min(K, 500) if not args.skip_extras else 1
     eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(Ke)]
     torch.cuda.synchronize()
@@ -304,7 +306,7 @@ def run_ours(args):
         return
 
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and not args.skip_extras and world == 1:
         import oracle
         flops_s, times = cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)
         cpu = {"value": flops_s / min(times) / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
@@ -474,6 +476,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time only the MLP step (for profiler captures)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="host-time budget of the reference arm (sets its per-step sample)")
     args = ap.parse_args(argv)

@@ -4,7 +4,14 @@ the accuracy bar for bf16 results.
 Accuracy bar (bf16 inputs, fp32 accumulation, compared with the fp64
 oracle on the same input bytes):
     relative Frobenius error  ||got - ref||_F / ||ref||_F  <= 5e-3
-    max |got - ref|                                         <= 2e-2 * RMS(ref)
+    elementwise |got - ref|  <= 2e-2 * RMS(ref) + u * |ref|
+where u is the unit roundoff of the output format: 2^-9 for a bf16 output,
+0 for an fp32 output.  The 2e-2 * RMS term bounds the accumulated error of
+the fp32 result; a bf16 output then rounds each element to nearest, which
+by itself can move it by half an ulp (up to 2^-9 |y|) -- more than
+2e-2 * RMS whenever |y| exceeds about 10 RMS, as in the positive tail of a
+GeLU output.  Tests that have both outputs also check that the bf16 output
+is exactly the round-to-nearest-even of the fp32 one.
 Integer-valued fp32 inputs must match exactly.
 """
 import numpy as np
@@ -56,9 +63,21 @@ def errors(got, ref):
     return rel, mx, rms
 
 
-def assert_bf16_parity(got, ref, what=""):
+BF16_UNIT_ROUNDOFF = 2.0 ** -9
+
+
+def assert_bf16_parity(got, ref, what="", out_bf16=True):
+    """Check a result of bf16 inputs with fp32 accumulation against the fp64
+    oracle (see the module docstring for the bar)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
     rel, mx, rms = errors(got, ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     assert rel <= REL_FRO_TOL, f"{what}: relative Frobenius error {rel:.3e} > {REL_FRO_TOL}"
-    assert mx <= MAX_ERR_RMS_TOL * rms, f"{what}: max |err| {mx:.3e} > {MAX_ERR_RMS_TOL} * RMS {rms:.3e}"
+    u = BF16_UNIT_ROUNDOFF if out_bf16 else 0.0
+    excess = np.abs(got - ref) - (MAX_ERR_RMS_TOL * rms + u * np.abs(ref))
+    worst = int(np.argmax(excess)) if excess.size else 0
+    assert excess.size == 0 or excess.flat[worst] <= 0, (
+        f"{what}: |err| {abs(got.flat[worst] - ref.flat[worst]):.3e} at ref {ref.flat[worst]:.4e} "
+        f"exceeds {MAX_ERR_RMS_TOL} * RMS {rms:.3e} + {u:.2e} * |ref|")
     return rel, mx, rms
