@@ -82,6 +82,7 @@ class ClockSampler:
         self.error = None
 
     def __enter__(self):
+        self._smi = None
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -90,9 +91,30 @@ class ClockSampler:
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
             self._thread = threading.Thread(target=self._run, daemon=True)
             self._thread.start()
-        except Exception as e:  # no NVML: report the gap instead of guessing
+        except Exception as e:  # no NVML module: sample through nvidia-smi
             self.error = repr(e)
+            self._start_smi()
         return self
+
+    def _start_smi(self):
+        import subprocess
+        import torch
+        uuid = str(getattr(torch.cuda.get_device_properties(self.device), "uuid", ""))
+        sel = []
+        if uuid:
+            sel = ["-i", uuid if uuid.upper().startswith("GPU-") else "GPU-" + uuid]
+        q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "20"]
+                + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.0)  # let the sampler start before the timed region
+        except OSError as e:
+            self.error = repr(e)
+            self._smi = None
+        self._t0 = time.time()
 
     def _handle_for(self, nv):
         # CUDA and NVML number devices differently; match by UUID.
@@ -121,9 +143,43 @@ class ClockSampler:
         self._stop.set()
         if self._thread:
             self._thread.join()
+        if self._smi is not None:
+            t1 = time.time()
+            time.sleep(0.1)
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=10)
+            self._smi_summary = self._parse_smi(out, self._t0, t1)
         return False
 
+    @staticmethod
+    def _parse_smi(text, t0, t1):
+        import datetime
+        rows, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                mhz, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            rows.append(mhz)
+            maxes.append(mx)
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not rows:
+            return None
+        return {"sm_mhz": statistics.median(rows), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi"}
+
     def summary(self):
+        if getattr(self, "_smi_summary", None):
+            return self._smi_summary
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
                     "samples": 0, "error": self.error}
@@ -143,7 +199,8 @@ class ClockSampler:
             seen |= int(r)
         reasons = sorted(k for k, bit in names.items() if seen & bit and k != "gpu_idle")
         return {"sm_mhz": statistics.median(m for m, _ in self.samples),
-                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml"}
 
 
 # ------------------------------------------------------------ helpers ------
@@ -285,13 +342,10 @@ def run_ours(args):
     e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
 
     # --------------------------------------------------- max over ranks -----
-    t = torch.tensor([dev_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dev_ms, e2e_ms = float(t[0]), float(t[1])
+    dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], dev, world)
     ms_per_step = dev_ms / K
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops_step, ms_per_step, world) / 1e12
+    e2e_value = whole_job_rate(flops_step, e2e_ms, world) / 1e12
 
     dom_ms, dom_flops, dom_name = ((k1_ms, flops_k1, "gemm column + GeLU (X.W1)")
                                    if k1_ms >= k2_ms else
@@ -354,15 +408,47 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank timings over all ranks (host-side
+    bookkeeping only; the replicas exchange no data)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(work_per_rank_step, ms_per_step_max, world):
+    """Units of work all ranks completed per second, timed by the slowest
+    rank (weak scaling: every replica does the same work per step)."""
+    return world * work_per_rank_step / (ms_per_step_max * 1e-3)
+
+
+def kernel_source_sha():
+    """Short hash of the CUDA sources, to tie profiler counters to a build."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "tensor_sharded_linear_02_b300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _profile_traffic(workload):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu
-    capture of the current kernel build, or None when there is none."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    capture, or None when there is none or the kernels changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
-            return json.load(fh).get(workload)
+            entry = json.load(fh).get(workload)
     except (OSError, ValueError):
         return None
+    if not entry or entry.get("source_sha") != kernel_source_sha():
+        return None
+    return entry.get("bytes")
 
 
 def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
@@ -471,7 +557,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)

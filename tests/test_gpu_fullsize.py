@@ -1,0 +1,125 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+bench uses.  The GPU computes the whole problem; the fp64 oracle computes a
+seeded sample of rows (every output row depends only on its own input row,
+so a sampled row is checked exactly as it would be in the full problem).
+Properties that hold at any size (shard outputs == concat columns bit for
+bit, sharded == unsharded, run-to-run identity) are checked on everything.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import assert_bf16_parity, bf16_dev_to_f64, dev_bits, dev_to_f64, to_dev_bf16
+from tensor_sharded_linear_02_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from tensor_sharded_linear_02_b300 import binding
+    binding.lib()
+    return binding
+
+
+def _rows(M, k, seed):
+    rng = np.random.default_rng(seed)
+    r = np.sort(rng.choice(M, size=k, replace=False))
+    r[0], r[-1] = 0, M - 1  # first and last row (ragged tile edges) always in
+    return np.unique(r)
+
+
+def _mlp_case(tp, dev, M, d, f, n_list, std, sample, seed):
+    import torch
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(seed, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(seed, 1), std)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(seed, 2), std)
+    X, W1, W2 = (to_dev_bf16(b, dev) for b in (xb, w1b, w2b))
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    rows = _rows(M, sample, seed)
+    Xs = oracle.bf16_to_f64(xb[rows])
+    W1d, W2d = oracle.bf16_to_f64(w1b), oracle.bf16_to_f64(w2b)
+    for n in n_list:
+        Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n)
+        assert tp.tp_get_device_status() == tp.TP_OK
+        got = bf16_dev_to_f64(Y[torch.from_numpy(rows).to(dev)])
+        ref = oracle.mlp_block(Xs, W1d, W2d, n)
+        assert_bf16_parity(got, ref, f"MLP {M}x{d}x{f} N={n} sampled rows")
+        H = ws[: M * f * 2].view(torch.bfloat16).view(M, f)
+        Hs = bf16_dev_to_f64(H[torch.from_numpy(rows).to(dev)])
+        Href, _ = oracle.column_linear(Xs, W1d, n, act="gelu")
+        assert_bf16_parity(Hs, Href, f"hidden H N={n} sampled rows")
+        Y2 = torch.empty_like(Y)
+        tp.tp_mlp_block(X, W1, W2, Y2, ws, n_shards=n)
+        assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+
+
+def test_gpt_mlp_block(tp, cuda_device):
+    """GPT-style MLP block: X [4096, 4096], W1 [4096, 16384], W2 [16384, 4096]
+    ~ N(0, 0.02), N = 8."""
+    _mlp_case(tp, cuda_device, 4096, 4096, 16384, [8], 0.02, sample=24, seed=3)
+
+
+def test_wide_mlp_shard_sweep(tp, cuda_device):
+    """Wide MLP block X [4096, 8192], W1 [8192, 28672], W2 [28672, 8192]
+    ~ N(0, 0.01), every shard count N in {1, 2, 4, 8, 16}."""
+    _mlp_case(tp, cuda_device, 4096, 8192, 28672, [1, 2, 4, 8, 16], 0.01, sample=8, seed=5)
+
+
+def test_attention_projections(tp, cuda_device):
+    """QKV projection X [8192, 4096] . Wqkv [4096, 12288] split into 8 head
+    groups of 4 heads (Q|K|V column blocks), and the output projection
+    C [8192, 4096] . Wo [4096, 4096] split by rows into 8 with the partials
+    summed on the device."""
+    import torch
+    dev = cuda_device
+    M, d, n, G = 8192, 4096, 8, 3
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(4, 0), 1.0)
+    wqkv = inputs.bf16_normal((d, G * d), inputs.stream_seed(4, 1), 0.02)
+    cb = inputs.bf16_normal((M, d), inputs.stream_seed(4, 2), 1.0)
+    wo = inputs.bf16_normal((d, d), inputs.stream_seed(4, 3), 0.02)
+    X, Wqkv, C, Wo = (to_dev_bf16(b, dev) for b in (xb, wqkv, cb, wo))
+    QKV = torch.empty(M, G * d, dtype=torch.bfloat16, device=dev)
+    loc = torch.empty(n, M, G * d // n, dtype=torch.bfloat16, device=dev)
+    tp.tp_column_linear_grouped(X, Wqkv, QKV, loc, n_shards=n, col_groups=G)
+    O = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    tp.tp_row_linear(C, Wo, O, None, n_shards=n)
+    cat = torch.empty_like(QKV)
+    tp.tp_shard_concat_grouped(loc, cat, col_groups=G)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    # all sizes: the standalone concat of the shard outputs rebuilds the fused one
+    assert torch.equal(cat.view(torch.int16), QKV.view(torch.int16))
+    rows = _rows(M, 16, 4)
+    ridx = torch.from_numpy(rows).to(dev)
+    ref_qkv, ref_loc = oracle.column_linear(oracle.bf16_to_f64(xb[rows]),
+                                            oracle.bf16_to_f64(wqkv), n, col_groups=G)
+    assert_bf16_parity(bf16_dev_to_f64(QKV[ridx]), ref_qkv, "QKV sampled rows")
+    assert_bf16_parity(bf16_dev_to_f64(loc[:, ridx]), ref_loc, "QKV head-group shards")
+    ref_o, _ = oracle.row_linear(oracle.bf16_to_f64(cb[rows]), oracle.bf16_to_f64(wo), n)
+    assert_bf16_parity(bf16_dev_to_f64(O[ridx]), ref_o, "Wo row split sampled rows")
+
+
+def test_standalone_reduce_sweep(tp, cuda_device):
+    """N fp32 partials [4096, 8192] -> bf16 for N in {1, 2, 4, 8, 16}, every
+    element checked against the oracle's double sum."""
+    import torch
+    dev = cuda_device
+    rows, cols = 4096, 8192
+    P16 = inputs.f32_normal((16, rows, cols), 4242)
+    Pd = torch.from_numpy(P16).to(dev)
+    for n in (1, 2, 4, 8, 16):
+        Yb = torch.empty(rows, cols, dtype=torch.bfloat16, device=dev)
+        Yf = torch.empty(rows, cols, dtype=torch.float32, device=dev)
+        tp.tp_shard_reduce(Pd[:n], Yb)
+        tp.tp_shard_reduce(Pd[:n], Yf)
+        assert tp.tp_get_device_status() == tp.TP_OK
+        ref = oracle.shard_reduce(P16[:n])
+        got = dev_to_f64(Yf)
+        abs_sum = np.zeros((rows, cols))
+        for i in range(n):
+            abs_sum += np.abs(P16[i])
+        bound = (n - 1) * 2.0 ** -24 * abs_sum
+        assert np.all(np.abs(got - ref) <= bound + 1e-30), f"reduce N={n}"
+        np.testing.assert_array_equal(dev_bits(Yb), oracle.f64_to_bf16(got).view(np.int16))
