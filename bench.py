@@ -430,7 +430,8 @@ def kernel_source_sha():
     import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "tensor_sharded_linear_02_b300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "tensor_sharded_linear_02_b300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cuh")) + [os.path.join(csrc, "tp_api.cu")]):
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())

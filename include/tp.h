@@ -218,6 +218,38 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y,
                        tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
 
 /*
+ * MLP block without a caller-provided workspace.  (No counterpart on the
+ * pages: this is a property of the library's memory handling, not of the
+ * method.)
+ *
+ * Same computation, arguments and errors as tp_mlp_block, minus ws and
+ * ws_bytes.  It is meant for callers that cannot allocate device memory when
+ * they call: a serving loop that must not call cudaMalloc once it is running
+ * (cudaMalloc can synchronise the whole device and stall other streams), or
+ * a host framework that owns all device memory through its own pool and
+ * hands the library only its input and output tensors.  The hidden
+ * activation H is kept instead in a fixed array inside the library's device
+ * image, TP_STATIC_WS_BYTES bytes, which every GPU that loads the library
+ * holds until the process exits.  The call allocates nothing.
+ *   - Limit: M * f * sizeof(in_t) <= TP_STATIC_WS_BYTES (32 MiB: for bf16,
+ *     for example, M = 2048 tokens with f up to 8192); larger problems
+ *     return TP_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress, with that device current) and
+ *     caches it; make that first call before any stream capture.
+ *   - Every call on a device uses the same array, which keeps what the last
+ *     call left there.  Nothing in it needs to start at zero (each call
+ *     writes all of H before reading it), but calls whose kernels overlap
+ *     on the GPU -- on different streams, or from different host threads --
+ *     race on it: order them on one stream or with events.
+ */
+#define TP_STATIC_WS_BYTES (32u << 20)
+
+tp_status tp_mlp_block_static_ws(const void *X, const void *W1, const void *W2, void *Y,
+                                 int64_t M, int64_t d, int64_t f, int n_shards,
+                                 tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
  * Synchronises stream s, then reads and clears the current device's status
  * word.  Returns TP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up
  * a bounded wait since the last call (its outputs are then invalid),

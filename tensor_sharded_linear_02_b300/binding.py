@@ -21,6 +21,7 @@ TP_F32, TP_BF16 = 0, 1
 TP_SPLIT_COLS, TP_SPLIT_ROWS = 0, 1
 TP_ACT_NONE, TP_ACT_GELU = 0, 1
 TP_MAX_SHARDS = 64
+TP_STATIC_WS_BYTES = 32 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,8 @@ SIGNATURES = {
     "tp_mlp_block_workspace_size": ([_i64, _i64, _int], ctypes.c_size_t),
     "tp_mlp_block": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i64, _i64, _i64, _int, _int,
                       _int, _vp], _int),
+    "tp_mlp_block_static_ws": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
+                               _int),
     "tp_get_device_status": ([_vp], _int),
     "tp_selftest_bounded_wait": ([ctypes.c_uint64, _vp], _int),
     "tp_status_string": ([_int], ctypes.c_char_p),
@@ -184,6 +187,17 @@ def tp_mlp_block(X, W1, W2, Y, ws, n_shards=1, stream=None):
                             ws.numel() * ws.element_size(), M, d, f, n_shards,
                             _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
     _check("tp_mlp_block", st)
+
+
+def tp_mlp_block_static_ws(X, W1, W2, Y, n_shards=1, stream=None):
+    """tp_mlp_block with the library's fixed scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    M, d = X.shape
+    f = W1.shape[1]
+    st = lib().tp_mlp_block_static_ws(_ptr(X), _ptr(W1), _ptr(W2), _ptr(Y), M, d, f, n_shards,
+                                      _dtype_code(X.dtype), _dtype_code(Y.dtype),
+                                      _stream(stream))
+    _check("tp_mlp_block_static_ws", st)
 
 
 def tp_get_device_status(stream=None) -> int:

@@ -2,9 +2,9 @@
 
     python -m tensor_sharded_linear_02_b300.build [--force] [--verbose]
 
-The library is one translation unit (csrc/tp_api.cu includes the kernel
-headers), linked against the static CUDA runtime so that the only runtime
-dependency is the driver.
+The library is csrc/tp_api.cu (which includes the kernel headers) plus
+csrc/tp_static_ws.cu, linked against the static CUDA runtime so that the
+only runtime dependency is the driver.
 """
 from __future__ import annotations
 
@@ -18,6 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libtp_b300.so")
 MAIN = os.path.join(HERE, "csrc", "tp_api.cu")
+STATIC_WS = os.path.join(HERE, "csrc", "tp_static_ws.cu")
 
 NVCC_FLAGS = [
     "-O3", "-std=c++17",
@@ -36,7 +37,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return ([MAIN] + glob.glob(os.path.join(HERE, "csrc", "*.cuh"))
+    return ([MAIN, STATIC_WS] + glob.glob(os.path.join(HERE, "csrc", "*.cuh"))
             + [os.path.join(ROOT, "include", "tp.h")])
 
 
@@ -46,7 +47,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not (force or stale):
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [_nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + [MAIN, "-o", tmp]
+    cmd = ([_nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else [])
+           + [MAIN, STATIC_WS, "-o", tmp])
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB
