@@ -9,8 +9,9 @@
 // issued by one thread -> fp32 accumulator in tensor memory -> tcgen05.ld by
 // the epilogue warps -> optional GeLU -> bf16 (RNE) or fp32 -> global store.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
-// MMA issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
+// MMA issuer, warps 2..9 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31,
+// warps 2..5 the first 128 accumulator columns, warps 6..9 the last 128).
 //
 // Two kernels:
 //   gemm_persistent_kernel  one CTA per SM walks work units (tile, k-group);
@@ -23,10 +24,13 @@
 //   gemm_cluster_sum_kernel  for outputs with too few tiles to fill the GPU:
 //       the S CTAs of a cluster share one output tile, CTA r accumulates the
 //       r-th contiguous slice of the K blocks (with K/n a multiple of the
-//       block depth and S dividing n, slice r is exactly shard group r), the
-//       fp32 partial tiles are parked in shared memory and CTA r adds rows
-//       [r*128/S, (r+1)*128/S) of all S partials, in ascending slice order,
-//       through distributed shared memory before the epilogue.
+//       block depth and S dividing n, slice r is exactly shard group r).  CTA
+//       r owns rows [r*128/S, (r+1)*128/S) of the tile.  Once every CTA of the
+//       cluster has finished its main loop (a cluster barrier: from then on no
+//       ring is in use), every CTA stores the fp32 partial rows it holds into
+//       slot `its rank` of the owner's shared memory (distributed shared
+//       memory stores), and after a second barrier each owner adds its S
+//       slots in ascending slice order.
 #pragma once
 
 #include "tp_device.cuh"
@@ -43,7 +47,13 @@ constexpr int B_CHUNK_N = 64;                   // N columns per TMA box (128 by
 constexpr int B_CHUNK_BYTES = BK * B_CHUNK_N * 2;  // 8 KiB
 constexpr int B_STAGE_BYTES = BK * BN * 2;      // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int EPI_WARPS = 4;
+#ifndef TP_EPI_WARPS
+#define TP_EPI_WARPS 8
+#endif
+// Epilogue warps: a multiple of 4 (each TMEM lane quadrant is read by
+// EPI_WARPS/4 warps, each taking an equal share of the columns).
+constexpr int EPI_WARPS = TP_EPI_WARPS;
+constexpr int EPI_COL_CHUNKS = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int RED_LD = BN + 4;  // fp32 row pitch of the parked partial tile (bank spread)
 
@@ -315,7 +325,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int q = warp & 3;                             // TMEM lane quadrant
+        const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;  // first 32-column chunk
         int local = 0;
         for (int u = blockIdx.x; u < a.num_units; u += gridDim.x, ++local) {
             const int acc = local & 1;
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int row = mt * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + c * 32, r);
                 tmem_ld_wait();
@@ -393,46 +404,63 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;
         if (mbar_wait_warp(smem_u32(&bars->acc_full[0]), 0, limit, &bars->abort,
-                           SITE_EPI_ACC_FULL)) {
+                           SITE_EPI_ACC_FULL))
             tc_fence_after();
-            // Every MMA has completed, so the ring is free: park the partial.
-            fence_proxy_async_smem();
-            const int rit = q * 32 + lane;  // row in tile
-            float *dst = red + rit * RED_LD;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    }
+
+    // Every CTA of the cluster has finished its main loop: from here on no
+    // ring is in use by TMA or MMA, so each can take parked partial rows.
+    cluster_sync_all();
+
+    if (warp >= 2 && !bars->abort) {
+        // Push: row `rit` of this CTA's fp32 partial goes to slot `rank` of
+        // its owner's parking area [S][BM/S][RED_LD] (local or remote).
+        fence_proxy_async_smem();
+        const int q = warp & 3;
+        const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;
+        const int rows_per = BM / S;
+        const int rit = q * 32 + lane;  // row in tile
+        const int owner = rit / rows_per;
+        const int slot_row = rank * rows_per + (rit - owner * rows_per);
+        float *dst = red + slot_row * RED_LD;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c * 32, r);
-                tmem_ld_wait();
+        for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    *reinterpret_cast<float4 *>(dst + c * 32 + v * 4) =
-                        make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
-                                    __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
+            for (int v = 0; v < 8; ++v) {
+                const float4 val =
+                    make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
+                                __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
+                float *p = dst + c * 32 + v * 4;
+                if (owner == rank)
+                    *reinterpret_cast<float4 *>(p) = val;
+                else
+                    dsmem_st_f4(dsmem_map(smem_u32(p), static_cast<uint32_t>(owner)), val);
             }
         }
     }
 
-    // Every CTA of the cluster has parked its partial.
+    // Every CTA of the cluster has delivered its partial rows.
     cluster_sync_all();
 
     if (warp >= 2) {
+        // Owner: rows [rank*BM/S, (rank+1)*BM/S) of the tile, S slots each,
+        // added in ascending slice order from local shared memory.
         const int rows_per = BM / S;
-        const int r0 = rank * rows_per;
-        const uint32_t red_base = smem_u32(red);
-        for (int rr = r0 + (warp - 2); rr < r0 + rows_per; rr += EPI_WARPS) {
-            const int row = mt * BM + rr;
-            // lane handles 8 consecutive columns: BN / 8 = 32 vectors per row
-            const int cl = lane * 8;
-            const uint32_t off = static_cast<uint32_t>((rr * RED_LD + cl) * 4);
-            float4 s0 = dsmem_ld_f4(dsmem_map(red_base + off, 0));
-            float4 s1 = dsmem_ld_f4(dsmem_map(red_base + off + 16, 0));
+        const int cl = lane * 8;  // 8 consecutive columns per lane, BN = 32 * 8
+        for (int rr = warp - 2; rr < rows_per; rr += EPI_WARPS) {
+            const int row = mt * BM + rank * rows_per + rr;
+            const float *src = red + rr * RED_LD + cl;
+            float4 s0 = *reinterpret_cast<const float4 *>(src);
+            float4 s1 = *reinterpret_cast<const float4 *>(src + 4);
             for (int p = 1; p < S; ++p) {
-                const float4 t0 = dsmem_ld_f4(dsmem_map(red_base + off, p));
-                const float4 t1 = dsmem_ld_f4(dsmem_map(red_base + off + 16, p));
+                const float *sp = src + p * rows_per * RED_LD;
+                const float4 t0 = *reinterpret_cast<const float4 *>(sp);
+                const float4 t1 = *reinterpret_cast<const float4 *>(sp + 4);
                 s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
                 s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
             }
@@ -444,7 +472,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
 
-    // No CTA may leave while a peer still reads its shared memory.
+    // No CTA leaves while a peer could still be writing into its shared memory.
     cluster_sync_all();
     tc_fence_before();
     __syncthreads();

@@ -256,6 +256,12 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta_
     return r;
 }
 
+__device__ __forceinline__ void dsmem_st_f4(uint32_t cluster_addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t cluster_addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
