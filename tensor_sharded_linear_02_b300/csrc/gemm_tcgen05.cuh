@@ -4,49 +4,69 @@
 //   A  row-major [M, K]   (X, or the hidden activation H)  -> K-major operand
 //   B  row-major [K, N]   (the weight W as stored)          -> MN-major operand
 //
-// Data path: TMA (128-byte swizzle) -> 4-stage shared-memory ring (mbarrier
-// full/empty pairs) -> tcgen05.mma.kind::f16, 128 x 256 x 16 per instruction,
-// issued by one thread -> fp32 accumulator in tensor memory -> tcgen05.ld by
-// the epilogue warps -> optional GeLU -> bf16 (RNE) or fp32 -> global store.
+// Every kernel runs on CTA pairs (clusters of 2, or of 2*S for the split
+// kernel) and issues tcgen05.mma.cta_group::2: one 256 x 256 output tile per
+// pair, 256 x 256 x 16 per instruction.  The even CTA of a pair stages A rows
+// 0..127 and B columns 0..127 of the tile, the odd CTA rows 128..255 and
+// columns 128..255; the tensor cores of both SMs read B from both shared
+// memories, so each SM stages half of B and only its own rows of A.  The
+// fp32 accumulator rows 0..127 live in the even CTA's tensor memory (TMEM),
+// rows 128..255 in the odd CTA's.
 //
-// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
-// MMA issuer, warps 2..9 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31,
-// warps 2..5 the first 128 accumulator columns, warps 6..9 the last 128).
+// Data path per CTA: TMA (128-byte swizzle) -> STAGES-deep shared-memory ring
+// of 32 KiB stages; the TMA bytes of both CTAs are counted on the even CTA's
+// `full` barrier; one thread of the even CTA issues the MMAs and releases a
+// stage in both CTAs with a multicast commit; the epilogue warps of each CTA
+// read its own TMEM (tcgen05.ld), apply the optional GeLU, round to bf16
+// (RNE) or keep fp32, and store.
+//
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner (and
+// MMA issuer in the even CTA), warps 2..9 = epilogue (warp w reads TMEM lanes
+// 32*(w%4)..+31; warps 2..5 take the first 128 accumulator columns, warps
+// 6..9 the last 128).
 //
 // Two kernels:
-//   gemm_persistent_kernel  one CTA per SM walks work units (tile, k-group);
-//       the accumulator is double-buffered in TMEM (2 x 256 columns) so the
-//       epilogue of one tile overlaps the main loop of the next.  k-group g
-//       selects shard g's K range through the 3-D tensor maps and its output
-//       goes to out + g * out_group_stride (per-shard partials); with one
-//       k-group the K loop walks shard 0's rows, then shard 1's, ..., so the
-//       row-parallel partial sums are added inside the accumulator.
+//   gemm_persistent_kernel  one pair per two SMs walks work units (tile,
+//       k-group); the accumulator is double-buffered in TMEM (2 x 256
+//       columns) so the epilogue of one tile overlaps the main loop of the
+//       next.  k-group g selects shard g's K range through the 3-D tensor
+//       maps and its output goes to out + g * out_group_stride (per-shard
+//       partials); with one k-group the K loop walks shard 0's rows, then
+//       shard 1's, ..., so the row-parallel partial sums are added inside the
+//       accumulator.
 //   gemm_cluster_sum_kernel  for outputs with too few tiles to fill the GPU:
-//       the S CTAs of a cluster share one output tile, CTA r accumulates the
-//       r-th contiguous slice of the K blocks (with K/n a multiple of the
-//       block depth and S dividing n, slice r is exactly shard group r).  CTA
-//       r owns rows [r*128/S, (r+1)*128/S) of the tile.  Once every CTA of the
-//       cluster has finished its main loop (a cluster barrier: from then on no
+//       the S pairs of a cluster share one output tile, pair p accumulates
+//       the p-th contiguous slice of the K blocks (with K/n a multiple of the
+//       block depth and S dividing n, slice p is exactly shard group p).  The
+//       S CTAs holding the same 128 rows (one per pair) split them: CTA of
+//       pair p owns rows [p*128/S, (p+1)*128/S) of that half.  Once every
+//       main loop of the cluster is done (a cluster barrier: from then on no
 //       ring is in use), every CTA stores the fp32 partial rows it holds into
-//       slot `its rank` of the owner's shared memory (distributed shared
+//       slot `its pair` of the owner's shared memory (distributed shared
 //       memory stores), and after a second barrier each owner adds its S
-//       slots in ascending slice order.
+//       slots in ascending slice order.  The sum never touches HBM.
 #pragma once
 
 #include "tp_device.cuh"
 
 namespace tpk {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int BM = 128;              // accumulator rows held by one CTA
+constexpr int PAIR_M = 2 * BM;       // rows of a pair tile
+constexpr int BN = 256;              // columns of a tile (accumulator width)
+constexpr int BN_HALF = BN / 2;      // B columns one CTA stages
+constexpr int BK = 64;               // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KiB
-constexpr int B_CHUNK_N = 64;                   // N columns per TMA box (128 bytes)
-constexpr int B_CHUNK_BYTES = BK * B_CHUNK_N * 2;  // 8 KiB
-constexpr int B_STAGE_BYTES = BK * BN * 2;      // 32 KiB
+#ifndef TP_STAGES
+#define TP_STAGES 6
+#endif
+constexpr int STAGES = TP_STAGES;
+constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KiB
+constexpr int B_CHUNK_N = 64;                       // N columns per TMA box (128 bytes)
+constexpr int B_CHUNK_BYTES = BK * B_CHUNK_N * 2;   // 8 KiB
+constexpr int B_STAGE_BYTES = BK * BN_HALF * 2;     // 16 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t PAIR_STAGE_TX = 2 * STAGE_BYTES; // bytes both CTAs land per stage
 #ifndef TP_EPI_WARPS
 #define TP_EPI_WARPS 8
 #endif
@@ -56,8 +76,10 @@ constexpr int EPI_WARPS = TP_EPI_WARPS;
 constexpr int EPI_COL_CHUNKS = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int RED_LD = BN + 4;  // fp32 row pitch of the parked partial tile (bank spread)
+constexpr int STG_BYTES = 32 * 128;  // one epilogue warp's store box: 32 rows x 128 bytes
+static_assert(BM * RED_LD * 4 <= STAGES * STAGE_BYTES, "partial tile must fit in the ring");
 
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, true);
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, true);
 
 // A descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
 // B descriptor: MN-major, 128-byte swizzle; a 64-column chunk holds all BK
@@ -67,28 +89,35 @@ constexpr uint32_t B_LBO = B_CHUNK_BYTES;
 constexpr uint32_t B_SBO = 1024;
 
 struct SmemBarriers {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t full[STAGES];     // even CTA: TMA bytes of both CTAs of the pair
+    uint64_t empty[STAGES];    // both CTAs: stage consumed (multicast commit)
+    uint64_t acc_full[2];      // both CTAs: accumulator ready (multicast commit)
+    uint64_t acc_empty[2];     // even CTA: epilogue warps of both CTAs done
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
 };
 
-constexpr int GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// Shared memory: ring | EPI_WARPS store boxes (1024-byte aligned, for the
+// 128-byte swizzle) | barriers.
+constexpr int GEMM_SMEM_BYTES =
+    STAGES * STAGE_BYTES + EPI_WARPS * STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(sizeof(SmemBarriers) <= 256, "barrier block");
 
 struct GemmArgs {
     int M, N;
     int k_blocks;        // BK-deep blocks per k-group (ceil)
     int k_groups;        // 1, or the shard count for per-shard partial outputs
-    int m_tiles, n_tiles;
+    int m_tiles, n_tiles;  // pair tiles (PAIR_M x BN)
     int num_units;       // m_tiles * n_tiles * k_groups (persistent kernel)
-    int split;           // cluster size S (cluster kernel)
+    int split;           // pairs per cluster S (cluster kernel)
     void *out;           // [M, N] row-major
     int64_t out_group_stride;  // elements between k-group outputs
     int out_f32;         // 1: fp32 output, 0: bf16
     int act_gelu;
+    int tma_store;       // 1: the plain output goes through shared memory and TMA
+                         //    stores (tensor map tmC); 0: per-thread vector stores
     void *out_shards;    // optional shard-major copy (column split)
     int shard_sw;        // columns a shard owns in each column group
     int shard_gw;        // columns per column group
@@ -156,6 +185,105 @@ __device__ __forceinline__ void store_row_chunk32(const GemmArgs &a, int g, int 
     }
 }
 
+// Hands the accumulator back to the MMA issuer once this warp's tensor
+// memory reads are complete.
+__device__ __forceinline__ void release_accumulator(uint32_t acc_empty_addr) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(acc_empty_addr);
+}
+
+// Direct epilogue (per-thread 16-byte stores, one row per lane): used when
+// a shard-major copy is requested.  Columns [c0*32, c0*32 + 32*EPI_COL_CHUNKS)
+// of the accumulator at taddr.
+__device__ __forceinline__ void epilogue_direct(const GemmArgs &a, uint32_t taddr, int row,
+                                                int col_base, int c0, int g,
+                                                uint32_t acc_empty_addr) {
+#pragma unroll 1
+    for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        store_row_chunk32(a, g, row, col_base + c * 32, r);
+    }
+    release_accumulator(acc_empty_addr);
+}
+
+// Stages one 32-row x 128-byte box (8 16-byte chunks per row, held by lane =
+// row) in this warp's store buffer with the 128-byte swizzle (chunk c of row
+// r at position c ^ (r mod 8): conflict-free, 4 wavefronts per chunk column)
+// and sends it to global memory with one TMA store.
+__device__ __forceinline__ void stage_and_store_box(const CUtensorMap *tmC, uint32_t stg,
+                                                    const uint32_t (&pk)[32], int col, int row,
+                                                    int g) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+    __syncwarp();
+    const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row_addr + ((c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                     pk[4 * c + 3]);
+    fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmC, stg, col, row, g);
+        bulk_commit_group();
+    }
+}
+
+// TMA-store epilogue: the warp's 32 rows (starting at `row0`) and 128
+// accumulator columns (starting at `cofs` within the tile at `col_base`).
+// bf16 output: two 64-column boxes; fp32 output: four 32-column boxes.  The
+// accumulator is released as soon as its last tensor-memory load is done.
+// Rows >= M and columns >= N of a box are clipped by the TMA unit.
+__device__ __forceinline__ void epilogue_tma_store(const GemmArgs &a, const CUtensorMap *tmC,
+                                                   uint32_t taddr, uint32_t stg, int row0,
+                                                   int col_base, int cofs, int g,
+                                                   uint32_t acc_empty_addr) {
+    if (!a.out_f32) {
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + cofs + j * 64, r0);
+            tmem_ld_32x32b_x32(taddr + cofs + j * 64 + 32, r1);
+            tmem_ld_wait();
+            if (j == 1) release_accumulator(acc_empty_addr);
+            uint32_t pk[32];
+            if (a.act_gelu) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    pk[i] = pack_bf16x2(gelu_f32(__uint_as_float(r0[2 * i])),
+                                        gelu_f32(__uint_as_float(r0[2 * i + 1])));
+                    pk[16 + i] = pack_bf16x2(gelu_f32(__uint_as_float(r1[2 * i])),
+                                             gelu_f32(__uint_as_float(r1[2 * i + 1])));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                    pk[16 + i] =
+                        pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+                }
+            }
+            stage_and_store_box(tmC, stg, pk, col_base + cofs + j * 64, row0, g);
+        }
+    } else {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + cofs + j * 32, r);
+            tmem_ld_wait();
+            if (j == 3) release_accumulator(acc_empty_addr);
+            if (a.act_gelu) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gelu_f32(__uint_as_float(r[i])));
+            }
+            stage_and_store_box(tmC, stg, r, col_base + cofs + j * 32, row0, g);
+        }
+    }
+}
+
 __device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_tile, int &n_tile,
                                             int &g) {
     const int tiles = a.m_tiles * a.n_tiles;
@@ -166,50 +294,79 @@ __device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_til
 }
 
 // ---------------------------------------------------------------------------
-// Producer: one thread issues the TMA loads of k-blocks [kb0, kb1) of one
-// unit into the ring.  Returns false on abort.
+// Producer (one thread in each CTA of the pair): TMA loads of this CTA's
+// half of k-blocks [kb0, kb1) of one pair tile into its ring, counted on the
+// even CTA's full barrier (`full_remote` = its shared::cluster address for
+// stage 0; stages are 8 bytes apart).  The even CTA also announces the pair's
+// transaction bytes.  Returns false on abort.
 // ---------------------------------------------------------------------------
+struct ProducerState {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0;  // loads issued whose stage was not yet seen released
+};
+
 __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                                uint8_t *ring, SmemBarriers *bars, int &stage,
-                                                uint32_t &phase, uint32_t &issued_mask,
-                                                uint32_t &issued_parity, int m_tile, int n_tile,
-                                                int g, int kb0, int kb1, uint64_t limit) {
+                                                uint8_t *ring, SmemBarriers *bars,
+                                                uint32_t full_remote, bool leader, int half,
+                                                ProducerState &ps, int m_tile, int n_tile, int g,
+                                                int kb0, int kb1, uint64_t limit) {
+    const int row0 = m_tile * PAIR_M + half * BM;
+    const int col0 = n_tile * BN + half * BN_HALF;
     for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&bars->empty[stage]), phase ^ 1u, limit, &bars->abort,
-                               SITE_PRODUCER_EMPTY))
+        if (!mbar_wait_bounded(smem_u32(&bars->empty[ps.stage]), ps.phase ^ 1u, limit,
+                               &bars->abort, SITE_PRODUCER_EMPTY))
             return false;
-        const uint32_t fb = smem_u32(&bars->full[stage]);
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        uint8_t *sa = ring + stage * STAGE_BYTES;
+        if (leader) mbar_arrive_expect_tx(smem_u32(&bars->full[ps.stage]), PAIR_STAGE_TX);
+        const uint32_t fb = full_remote + ps.stage * 8;
+        uint8_t *sa = ring + ps.stage * STAGE_BYTES;
         uint8_t *sb = sa + A_STAGE_BYTES;
-        tma_load_3d(smem_u32(sa), tmA, fb, kb * BK, g, m_tile * BM);
+        tma_load_3d_pair(smem_u32(sa), tmA, fb, kb * BK, g, row0);
 #pragma unroll
-        for (int j = 0; j < BN / B_CHUNK_N; ++j)
-            tma_load_3d(smem_u32(sb + j * B_CHUNK_BYTES), tmB, fb, n_tile * BN + j * B_CHUNK_N,
-                        kb * BK, g);
-        issued_mask |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+        for (int j = 0; j < BN_HALF / B_CHUNK_N; ++j)
+            tma_load_3d_pair(smem_u32(sb + j * B_CHUNK_BYTES), tmB, fb, col0 + j * B_CHUNK_N,
+                             kb * BK, g);
+        ps.issued = 1;
+        if (++ps.stage == STAGES) {
+            ps.stage = 0;
+            ps.phase ^= 1u;
         }
     }
     return true;
 }
 
-// After an abort, wait (bounded) for every load the producer issued, so no
-// copy is still landing in shared memory when the CTA exits.
-__device__ __forceinline__ void producer_drain(SmemBarriers *bars, uint32_t issued_mask,
-                                               uint32_t issued_parity, uint64_t limit) {
-    for (int s = 0; s < STAGES; ++s)
-        if (issued_mask & (1u << s))
-            mbar_wait_drain(smem_u32(&bars->full[s]), (issued_parity >> s) & 1u, limit);
+// After the last load: wait until every stage of this CTA's ring has been
+// released by the MMA issuer.  The releases are multicast commits from the
+// even CTA; none may still be on its way when the CTA exits.
+__device__ __forceinline__ bool producer_tail(SmemBarriers *bars, ProducerState &ps,
+                                              uint64_t limit) {
+    for (int i = 0; i < STAGES; ++i) {
+        if (!mbar_wait_bounded(smem_u32(&bars->empty[ps.stage]), ps.phase ^ 1u, limit,
+                               &bars->abort, SITE_PRODUCER_EMPTY))
+            return false;
+        if (++ps.stage == STAGES) {
+            ps.stage = 0;
+            ps.phase ^= 1u;
+        }
+    }
+    return true;
 }
 
-// MMA issuer: accumulate k-blocks [kb0, kb1) into TMEM columns at d_tmem.
+// After an abort the loads this CTA issued are counted on the even CTA's
+// barrier, which this CTA cannot wait on; give them a fixed time to land
+// (far above any load latency) before the CTA may leave.
+__device__ __forceinline__ void producer_drain(const ProducerState &ps) {
+    if (!ps.issued) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+}
+
+// MMA issuer (even CTA): accumulate k-blocks [kb0, kb1) into TMEM columns at
+// d_tmem of both CTAs; each consumed stage is released in both CTAs.
 __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, int &stage,
-                                            uint32_t &phase, uint32_t d_tmem, int kb0, int kb1,
-                                            uint64_t limit) {
+                                            uint32_t &phase, uint32_t d_tmem, uint16_t pair_mask,
+                                            int kb0, int kb1, uint64_t limit) {
     for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, limit, &bars->abort,
                                SITE_MMA_FULL))
@@ -223,9 +380,9 @@ __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, i
             // B: advance 16 k-rows = two 8-row groups of 1024 bytes.
             const uint64_t da = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, A_SBO);
             const uint64_t db = smem_desc_sw128(sb + k * (UMMA_K / 8) * B_SBO, B_LBO, B_SBO);
-            umma_f16(d_tmem, da, db, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_f16_pair(d_tmem, da, db, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars->empty[stage]));
+        umma_commit_pair_mc(smem_u32(&bars->empty[stage]), pair_mask);
         if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -235,7 +392,7 @@ __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, i
 }
 
 __device__ __forceinline__ void mma_drain(SmemBarriers *bars, uint64_t limit) {
-    umma_commit(smem_u32(&bars->drain));
+    umma_commit_pair(smem_u32(&bars->drain));
     mbar_wait_drain(smem_u32(&bars->drain), 0, limit);
 }
 
@@ -243,8 +400,14 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_cols, int epi_arrivals,
-                                           const CUtensorMap *tmA, const CUtensorMap *tmB) {
+// Barrier init and TMEM allocation in both CTAs of every pair, then a
+// cluster barrier: no CTA sends bytes or arrivals to a peer barrier before
+// the peer has initialised it.  Then the programmatic-launch hand-off: the
+// next kernel of the stream may start launching, and this one waits for the
+// previous kernel to complete.
+__device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_cols,
+                                           const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                           const CUtensorMap *tmC, bool store_map) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -253,7 +416,7 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_col
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&bars->acc_full[i]), 1);
-            mbar_init(smem_u32(&bars->acc_empty[i]), epi_arrivals);
+            mbar_init(smem_u32(&bars->acc_empty[i]), 2 * EPI_WARPS);
         }
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
@@ -263,63 +426,86 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_col
     if (warp == 0 && (threadIdx.x & 31) == 0) {
         tma_prefetch_desc(tmA);
         tma_prefetch_desc(tmB);
+        if (store_map) tma_prefetch_desc(tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&bars->tmem_base), tmem_cols);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(&bars->tmem_base), tmem_cols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
+    // Everything above is private to this CTA pair, so it overlaps the tail
+    // of the previous kernel; the inputs (possibly that kernel's output) and
+    // the outputs are touched only after it has completed.
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
+}
+
+__device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, uint32_t tmem_cols) {
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no peer still reads this CTA's ring or signals its barriers
+    tc_fence_after();
+    if ((threadIdx.x >> 5) == 1) tmem_dealloc_pair(tmem_base, tmem_cols);
 }
 
 // ---------------------------------------------------------------------------
-// Persistent kernel.
+// Persistent kernel: cluster = one pair, grid = 2 x (pairs launched).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
-    SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(ring + STAGES * STAGE_BYTES);
+    uint8_t *staging = ring + STAGES * STAGE_BYTES;
+    SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(staging + EPI_WARPS * STG_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr uint32_t TMEM_COLS = 2 * BN;
 
-    gemm_setup(bars, TMEM_COLS, EPI_WARPS, &tmA, &tmB);
+    const int half = static_cast<int>(cluster_ctarank());  // 0 = even (leader), 1 = odd
+    const bool leader = half == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    gemm_setup(bars, TMEM_COLS, &tmA, &tmB, &tmC, a.tma_store != 0);
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+            const uint32_t full_remote = dsmem_map(smem_u32(&bars->full[0]), 0);
+            ProducerState ps;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+            for (int u = pair; u < a.num_units && ok; u += num_pairs) {
                 int mt, nt, g;
                 decode_unit(a, u, mt, nt, g);
-                ok = produce_kblocks(&tmA, &tmB, ring, bars, stage, phase, issued_mask,
-                                     issued_parity, mt, nt, g, 0, a.k_blocks, limit);
+                ok = produce_kblocks(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt,
+                                     nt, g, 0, a.k_blocks, limit);
             }
-            if (!ok) producer_drain(bars, issued_mask, issued_parity, limit);
+            if (ok) ok = producer_tail(bars, ps, limit);
+            if (!ok) producer_drain(ps);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (leader && lane == 0) {
             int stage = 0, local = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++local) {
+            for (int u = pair; u < a.num_units && ok; u += num_pairs, ++local) {
                 const int acc = local & 1;
                 const uint32_t acc_par = (local >> 1) & 1;
                 ok = mbar_wait_bounded(smem_u32(&bars->acc_empty[acc]), acc_par ^ 1u, limit,
                                        &bars->abort, SITE_MMA_ACC_EMPTY);
                 if (!ok) break;
                 tc_fence_after();
-                ok = mma_kblocks(ring, bars, stage, phase, tmem_base + acc * BN, 0, a.k_blocks,
-                                 limit);
+                ok = mma_kblocks(ring, bars, stage, phase, tmem_base + acc * BN, 0x3, 0,
+                                 a.k_blocks, limit);
                 if (!ok) break;
-                umma_commit(smem_u32(&bars->acc_full[acc]));
+                umma_commit_pair_mc(smem_u32(&bars->acc_full[acc]), 0x3);
             }
             if (!ok) mma_drain(bars, limit);
         }
@@ -327,8 +513,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else {
         const int q = warp & 3;                             // TMEM lane quadrant
         const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;  // first 32-column chunk
+        const uint32_t acc_empty_remote = dsmem_map(smem_u32(&bars->acc_empty[0]), 0);
+        const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
         int local = 0;
-        for (int u = blockIdx.x; u < a.num_units; u += gridDim.x, ++local) {
+        for (int u = pair; u < a.num_units; u += num_pairs, ++local) {
             const int acc = local & 1;
             const uint32_t acc_par = (local >> 1) & 1;
             if (!mbar_wait_warp(smem_u32(&bars->acc_full[acc]), acc_par, limit, &bars->abort,
@@ -337,68 +525,72 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             int mt, nt, g;
             decode_unit(a, u, mt, nt, g);
-            const int row = mt * BM + q * 32 + lane;
             const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-            for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c * 32, r);
-                tmem_ld_wait();
-                store_row_chunk32(a, g, row, nt * BN + c * 32, r);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[acc]));
+            const uint32_t release = acc_empty_remote + acc * 8;
+            if (a.tma_store)
+                epilogue_tma_store(a, &tmC, taddr, stg, mt * PAIR_M + half * BM + q * 32,
+                                   nt * BN, c0 * 32, g, release);
+            else
+                epilogue_direct(a, taddr, mt * PAIR_M + half * BM + q * 32 + lane, nt * BN, c0,
+                                g, release);
         }
+        if (lane == 0) bulk_wait0();  // every store box has left shared memory and landed
+        __syncwarp();
     }
 
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    gemm_teardown(tmem_base, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
-// Cluster split kernel: grid = S * tiles CTAs, cluster = S CTAs along x.
+// Cluster split kernel: grid = 2 * S * tiles CTAs, cluster = 2 * S CTAs along
+// x (S pairs; cluster rank 2p + h is half h of pair p).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_cluster_sum_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
-    SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(ring + STAGES * STAGE_BYTES);
+    uint8_t *staging = ring + STAGES * STAGE_BYTES;
+    SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(staging + EPI_WARPS * STG_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr uint32_t TMEM_COLS = BN;
 
     const int S = a.split;
     const int rank = static_cast<int>(cluster_ctarank());
-    const int tile = blockIdx.x / S;
+    const int p = rank >> 1;      // pair = K slice
+    const int half = rank & 1;    // which 128 rows of the tile
+    const bool leader = half == 0;
+    const int tile = blockIdx.x / (2 * S);
     const int mt = tile % a.m_tiles;
     const int nt = tile / a.m_tiles;
-    const int kb0 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * rank) / S);
-    const int kb1 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * (rank + 1)) / S);
+    const int kb0 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * p) / S);
+    const int kb1 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * (p + 1)) / S);
 
-    gemm_setup(bars, TMEM_COLS, EPI_WARPS, &tmA, &tmB);
+    gemm_setup(bars, TMEM_COLS, &tmA, &tmB, &tmC, a.tma_store != 0);
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
     float *red = reinterpret_cast<float *>(ring);  // parks the fp32 partial tile
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * p));
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
-            if (!produce_kblocks(&tmA, &tmB, ring, bars, stage, phase, issued_mask, issued_parity,
-                                 mt, nt, 0, kb0, kb1, limit))
-                producer_drain(bars, issued_mask, issued_parity, limit);
+            const uint32_t full_remote =
+                dsmem_map(smem_u32(&bars->full[0]), static_cast<uint32_t>(2 * p));
+            ProducerState ps;
+            if (!produce_kblocks(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt, nt, 0,
+                                 kb0, kb1, limit) ||
+                !producer_tail(bars, ps, limit))
+                producer_drain(ps);
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (leader && lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            if (mma_kblocks(ring, bars, stage, phase, tmem_base, kb0, kb1, limit))
-                umma_commit(smem_u32(&bars->acc_full[0]));
+            if (mma_kblocks(ring, bars, stage, phase, tmem_base, pair_mask, kb0, kb1, limit))
+                umma_commit_pair_mc(smem_u32(&bars->acc_full[0]), pair_mask);
             else
                 mma_drain(bars, limit);
         }
@@ -414,15 +606,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     cluster_sync_all();
 
     if (warp >= 2 && !bars->abort) {
-        // Push: row `rit` of this CTA's fp32 partial goes to slot `rank` of
-        // its owner's parking area [S][BM/S][RED_LD] (local or remote).
+        // Push: row `rit` of this CTA's fp32 partial (row half*128 + rit of
+        // the tile) goes to slot `p` of its owner's parking area
+        // [S][BM/S][RED_LD]; the owner is the CTA of the same half in pair
+        // rit / (BM/S).
         fence_proxy_async_smem();
         const int q = warp & 3;
         const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;
         const int rows_per = BM / S;
-        const int rit = q * 32 + lane;  // row in tile
-        const int owner = rit / rows_per;
-        const int slot_row = rank * rows_per + (rit - owner * rows_per);
+        const int rit = q * 32 + lane;
+        const int owner_p = rit / rows_per;
+        const int owner = 2 * owner_p + half;
+        const int slot_row = p * rows_per + (rit - owner_p * rows_per);
         float *dst = red + slot_row * RED_LD;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
@@ -435,11 +630,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const float4 val =
                     make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
                                 __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
-                float *p = dst + c * 32 + v * 4;
+                float *ptr = dst + c * 32 + v * 4;
                 if (owner == rank)
-                    *reinterpret_cast<float4 *>(p) = val;
+                    *reinterpret_cast<float4 *>(ptr) = val;
                 else
-                    dsmem_st_f4(dsmem_map(smem_u32(p), static_cast<uint32_t>(owner)), val);
+                    dsmem_st_f4(dsmem_map(smem_u32(ptr), static_cast<uint32_t>(owner)), val);
             }
         }
     }
@@ -447,18 +642,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // Every CTA of the cluster has delivered its partial rows.
     cluster_sync_all();
 
-    if (warp >= 2) {
-        // Owner: rows [rank*BM/S, (rank+1)*BM/S) of the tile, S slots each,
-        // added in ascending slice order from local shared memory.
+    if (warp >= 2 && !bars->abort) {
+        // Owner: rows [p*BM/S, (p+1)*BM/S) of half `half` of the tile, S
+        // slots each, added in ascending slice order from local shared memory.
         const int rows_per = BM / S;
         const int cl = lane * 8;  // 8 consecutive columns per lane, BN = 32 * 8
         for (int rr = warp - 2; rr < rows_per; rr += EPI_WARPS) {
-            const int row = mt * BM + rank * rows_per + rr;
+            const int row = mt * PAIR_M + half * BM + p * rows_per + rr;
             const float *src = red + rr * RED_LD + cl;
             float4 s0 = *reinterpret_cast<const float4 *>(src);
             float4 s1 = *reinterpret_cast<const float4 *>(src + 4);
-            for (int p = 1; p < S; ++p) {
-                const float *sp = src + p * rows_per * RED_LD;
+            for (int j = 1; j < S; ++j) {
+                const float *sp = src + j * rows_per * RED_LD;
                 const float4 t0 = *reinterpret_cast<const float4 *>(sp);
                 const float4 t1 = *reinterpret_cast<const float4 *>(sp + 4);
                 s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
@@ -472,12 +667,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
 
-    // No CTA leaves while a peer could still be writing into its shared memory.
-    cluster_sync_all();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    gemm_teardown(tmem_base, TMEM_COLS);
 }
 
 }  // namespace tpk

@@ -25,8 +25,32 @@ constexpr int64_t kInt32Max = 0x7FFFFFFF;
 
 struct DeviceInfo {
     int sm_count = 0;
+    int max_pairs = 0;          // clusters of 2 GEMM CTAs that fit at once
+    int max_clusters[5] = {};   // index log2(S): clusters of 2*S GEMM CTAs that fit at once
     bool ready = false;
 };
+
+// How many clusters of `size` GEMM CTAs can be resident at once (0 if the
+// size cannot be launched).
+int active_clusters(const void *kernel, int size) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(size), 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
 
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
@@ -46,6 +70,11 @@ tp_status device_info(DeviceInfo **out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM_BYTES) != cudaSuccess)
             return TP_ERR_CUDA;
+        d.max_pairs = active_clusters(reinterpret_cast<const void *>(gemm_persistent_kernel), 2);
+        if (d.max_pairs < 1) return TP_ERR_CUDA;
+        for (int l = 1; l <= 2; ++l)  // S = 2, 4 pairs: clusters of 4 and 8 CTAs
+            d.max_clusters[l] =
+                active_clusters(reinterpret_cast<const void *>(gemm_cluster_sum_kernel), 2 << l);
         d.ready = true;
     }
     *out = &d;
@@ -83,17 +112,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+// 3-D tensor map (bf16 unless f32), 128-byte swizzle, zero fill out of bounds.
 bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2) {
+               uint32_t b2, bool f32 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -135,13 +165,16 @@ struct GemmCall {
     bool allow_split;
 };
 
-// Cluster size for outputs with too few tiles to occupy the GPU: the largest
-// power of two S <= 8 with tiles * S <= SM count and at least one k-block
-// per CTA.  1 means the persistent kernel.
-int choose_split(int tiles, int k_blocks, int sm_count) {
+// Pairs per cluster for outputs with too few pair tiles to occupy the GPU:
+// the largest S in {2, 4} such that tiles * S clusters of 2*S CTAs are all
+// resident at once and each pair gets at least one k-block; 1 means the
+// persistent kernel.
+int choose_split(int tiles, int k_blocks, const DeviceInfo &dev) {
     int S = 1;
-    while (S * 2 <= 8 && static_cast<int64_t>(tiles) * S * 2 <= sm_count && S * 2 <= k_blocks)
-        S *= 2;
+    for (int l = 1; l <= 2; ++l) {
+        const int s2 = 1 << l;
+        if (tiles <= dev.max_clusters[l] && s2 <= k_blocks) S = s2;
+    }
     return S;
 }
 
@@ -158,12 +191,25 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     if (!encode_3d(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
         return TP_ERR_CUDA;
 
+    // Output viewed as [k_groups][M][N]; box = 32 rows x 128 bytes of one group.
+    CUtensorMap tmC;
+    const bool tma_store = c.out != nullptr && c.out_shards == nullptr;
+    std::memset(&tmC, 0, sizeof(tmC));
+    if (tma_store) {
+        const uint64_t es = c.out_f32 ? 4 : 2;
+        if (!encode_3d(&tmC, c.out, c.N, c.M, c.k_groups, c.N * es,
+                       (c.k_groups > 1 ? c.out_group_stride : c.M * c.N) * es,
+                       static_cast<uint32_t>(128 / es), 32, 1, c.out_f32))
+            return TP_ERR_CUDA;
+    }
+
     GemmArgs a{};
+    a.tma_store = tma_store ? 1 : 0;
     a.M = static_cast<int>(c.M);
     a.N = static_cast<int>(c.N);
     a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
     a.k_groups = c.k_groups;
-    a.m_tiles = static_cast<int>((c.M + BM - 1) / BM);
+    a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
     a.n_tiles = static_cast<int>((c.N + BN - 1) / BN);
     a.num_units = a.m_tiles * a.n_tiles * c.k_groups;
     a.out = c.out;
@@ -179,29 +225,31 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.wait_limit_ns = wait_limit_ns();
 
     const int tiles = a.m_tiles * a.n_tiles;
-    const int S = (c.allow_split && c.k_groups == 1) ? choose_split(tiles, a.k_blocks, dev->sm_count)
-                                                     : 1;
-    if (S > 1) {
-        a.split = S;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(tiles * S), 1, 1);
-        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(S);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, a) != cudaSuccess)
-            return TP_ERR_CUDA;
-        return launch_status();
-    }
-    a.split = 1;
-    const int grid = a.num_units < dev->sm_count ? a.num_units : dev->sm_count;
-    gemm_persistent_kernel<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(tmA, tmB, a);
+    const int S = (c.allow_split && c.k_groups == 1) ? choose_split(tiles, a.k_blocks, *dev) : 1;
+    a.split = S;
+    const int pairs = S > 1 ? tiles * S : (a.num_units < dev->max_pairs ? a.num_units
+                                                                         : dev->max_pairs);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(2 * S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the kernel's set-up (barriers, tensor
+    // memory, descriptor prefetch) overlaps the previous kernel's tail; it
+    // waits on the device (griddepcontrol.wait) before touching memory.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = S > 1
+                              ? cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, tmC, a)
+                              : cudaLaunchKernelEx(&cfg, gemm_persistent_kernel, tmA, tmB, tmC, a);
+    if (e != cudaSuccess) return TP_ERR_CUDA;
     return launch_status();
 }
 

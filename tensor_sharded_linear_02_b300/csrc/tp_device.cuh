@@ -32,6 +32,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream is still
+// running; `grid_dep_wait` blocks until that kernel has completed and its
+// memory operations are visible, so everything before it must touch no
+// global data the previous kernel could read or write.  `grid_dep_trigger`
+// lets the next kernel of the stream start launching (it still waits for
+// this one to complete before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -58,6 +71,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on a barrier that may belong to another CTA of the cluster (address
+// in the shared::cluster window, from mapa).  Used by the epilogue to hand a
+// drained accumulator back: the data it guards is tensor memory whose reads
+// were completed (tcgen05.wait::ld) and fenced before the arrive, so the
+// default release at CTA scope is enough and no global store has to drain.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -138,6 +160,102 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// Same load for a CTA pair that issues one tcgen05.mma.cta_group::2: the data
+// lands in this CTA's shared memory, the completed bytes are counted on the
+// barrier at `cluster_bar`, which may belong to the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t cluster_bar, int32_t c0, int32_t c1,
+                                                 int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// TMA tiled store of a box from this CTA's shared memory, tracked as a bulk
+// async group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until no committed bulk store of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 for a CTA pair (cta_group::2): one thread of the even CTA issues
+// M = 256 MMAs whose A rows 0..127 and B columns 0..N/2-1 come from its own
+// shared memory and A rows 128..255 and B columns N/2..N-1 from the peer's
+// (same offsets); accumulator rows 0..127 land in the even CTA's tensor
+// memory and rows 128..255 in the odd CTA's.  Allocation is collective over
+// one warp of each CTA of the pair.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in every CTA of `cta_mask` when
+// all pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Arrive on this CTA's barrier at `bar` when the pair MMAs issued so far by
+// this thread have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -274,10 +392,35 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t cluster_addr) {
 // ---------------------------------------------------------------------------
 // Numerics shared by the epilogues.
 // ---------------------------------------------------------------------------
-// Exact GeLU x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2, in fp32 with the
-// CUDA math library's erff.
+// Exact (erf-form) GeLU, x * Phi(x) with Phi(x) = (1 + erf(x / sqrt 2)) / 2,
+// in fp32.  erf is evaluated with the rational approximation of Abramowitz
+// and Stegun, "Handbook of Mathematical Functions" (1964), formula 7.1.28:
+// for z >= 0,
+//     erfc(z) = 1 - erf(z) ~ (1 + a1 z + a2 z^2 + ... + a6 z^6)^-16,
+// absolute error at most 3e-7.  With z = |x| / sqrt 2 and r = erfc(z),
+// Phi(x) = 1 - r/2 for x >= 0 and r/2 for x < 0.  Cost: 6 fused
+// multiply-adds for the polynomial, 4 squarings, one hardware reciprocal.
+// The error of Phi stays near 1e-6 (the approximation plus the rounding of
+// the 16th power), three orders of magnitude below the half-ulp (2^-9
+// relative) of the bf16 value the epilogue stores.  For z above ~20 the
+// 16th power overflows to +inf and r = 0, the correct limit.
 __device__ __forceinline__ float gelu_f32(float x) {
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+    const float z = fabsf(x) * 0.70710678118654752440f;
+    float p = fmaf(4.30638e-5f, z, 2.765672e-4f);
+    p = fmaf(p, z, 1.520143e-4f);
+    p = fmaf(p, z, 9.2705272e-3f);
+    p = fmaf(p, z, 4.22820123e-2f);
+    p = fmaf(p, z, 7.05230784e-2f);
+    p = fmaf(p, z, 1.0f);
+    p = p * p;  // ^2
+    p = p * p;  // ^4
+    p = p * p;  // ^8
+    p = p * p;  // ^16
+    float h;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
+    h *= 0.5f;  // erfc(z) / 2
+    const float phi = x >= 0.0f ? 1.0f - h : h;
+    return x * phi;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

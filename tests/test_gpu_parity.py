@@ -156,6 +156,42 @@ def test_column_linear_bf16(tp, cuda_device, M, K, N, n, act):
     np.testing.assert_array_equal(dev_bits(Yf.to(torch.bfloat16)), dev_bits(Y))
 
 
+def test_gelu_epilogue_accuracy(tp, cuda_device):
+    """The epilogue's GeLU against the fp64 oracle GeLU at every bf16 value
+    with |x| <= 12 (and a few beyond): W = [I_8 | I_8 | ...] makes X.W copy
+    X's entries exactly into an fp32 accumulator, so the fp32 output is
+    GeLU(x) itself.  The device evaluates erf with Abramowitz & Stegun 7.1.28
+    (absolute error <= 3e-7); with the rounding of its 16th power and of the
+    final products the bound used here is 1e-6 * max(1, |x|)."""
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_to_f64(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 12.0)
+    extra = oracle.bf16_to_f64(np.array([0x4200, 0xC200, 0x4300, 0xC300], dtype=np.uint16))
+    xb = np.concatenate([bits[keep], np.array([0x4200, 0xC200, 0x4300, 0xC300], np.uint16)])
+    xs = np.concatenate([vals[keep], extra])  # +-32, +-128 added
+    pad = (-xb.size) % 8
+    xb = np.concatenate([xb, np.zeros(pad, np.uint16)])
+    xs = np.concatenate([xs, np.zeros(pad)])
+    M = xb.size // 8
+    N = 8 * 33  # 264 columns: two column tiles, the second ragged
+    w = np.zeros((8, N), dtype=np.float64)
+    w[np.arange(N) % 8, np.arange(N)] = 1.0
+    wb = oracle.f64_to_bf16(w)
+    X, W = to_dev_bf16(xb.reshape(M, 8), cuda_device), to_dev_bf16(wb, cuda_device)
+    Yf = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+    tp.tp_column_linear(X, W, Yf, None, n_shards=1, act="gelu")
+    _status_ok(tp)
+    got = dev_to_f64(Yf)
+    xin = xs.reshape(M, 8)[:, np.arange(N) % 8]
+    ref = oracle.gelu(xin.ravel()).reshape(M, N)
+    err = np.abs(got - ref)
+    bound = 1e-6 * np.maximum(1.0, np.abs(xin))
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), (
+        f"GeLU({xin.flat[worst]}) = {got.flat[worst]!r}, oracle {ref.flat[worst]!r}")
+
+
 @pytest.mark.parametrize("M,K,G,n,sw", [(256, 128, 3, 4, 64), (130, 64, 3, 2, 8), (64, 32, 2, 8, 16)])
 def test_column_linear_head_groups(tp, cuda_device, M, K, G, n, sw):
     """Head-group split: shard i owns slice i of each of the G column blocks."""
