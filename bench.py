@@ -323,6 +323,9 @@ def run_ours(args):
     red = cat = None
     if not args.skip_extras:
         red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
+        red["sweep"] = {str(ns): bench_reduce(tp, dev, stream, peaks, K=min(K, 100), n=ns)["value"]
+                        for ns in (1, 2, 4, 16)}
+        red["sweep"]["8"] = red["value"]
         cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
 
     # --------------------------------------------------------------- e2e ----

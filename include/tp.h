@@ -210,7 +210,9 @@ size_t tp_mlp_block_workspace_size(int64_t M, int64_t f, tp_dtype t);
  *     i of H -- and is never gathered.
  * Two kernels on stream s: the column GEMM with the GeLU fused into its
  * epilogue, then the row GEMM with the shard sum fused into its fp32
- * accumulator.  Errors: as the two linears, plus TP_ERR_WORKSPACE.
+ * accumulator (the second launched so that its set-up overlaps the first's
+ * tail).
+ * Errors: as the two linears, plus TP_ERR_WORKSPACE.
  */
 tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y,
                        void *ws, size_t ws_bytes,

@@ -5,46 +5,54 @@
 //   B  row-major [K, N]   (the weight W as stored)          -> MN-major operand
 //
 // Every kernel runs on CTA pairs (clusters of 2, or of 2*S for the split
-// kernel) and issues tcgen05.mma.cta_group::2: one 256 x 256 output tile per
-// pair, 256 x 256 x 16 per instruction.  The even CTA of a pair stages A rows
-// 0..127 and B columns 0..127 of the tile, the odd CTA rows 128..255 and
-// columns 128..255; the tensor cores of both SMs read B from both shared
-// memories, so each SM stages half of B and only its own rows of A.  The
-// fp32 accumulator rows 0..127 live in the even CTA's tensor memory (TMEM),
-// rows 128..255 in the odd CTA's.
+// kernel) and issues tcgen05.mma.cta_group::2: one 256 x bn output tile per
+// pair (bn = 256 or 128), 256 x bn x 16 per instruction.  The even CTA of a
+// pair stages A rows 0..127 and B columns 0..bn/2-1 of the tile, the odd CTA
+// rows 128..255 and columns bn/2..bn-1; the tensor cores of both SMs read B
+// from both shared memories, so each SM stages half of B and only its own
+// rows of A.  The fp32 accumulator rows 0..127 live in the even CTA's tensor
+// memory (TMEM), rows 128..255 in the odd CTA's.
 //
-// Data path per CTA: TMA (128-byte swizzle) -> STAGES-deep shared-memory ring
-// of 32 KiB stages; the TMA bytes of both CTAs are counted on the even CTA's
-// `full` barrier; one thread of the even CTA issues the MMAs and releases a
-// stage in both CTAs with a multicast commit; the epilogue warps of each CTA
-// read its own TMEM (tcgen05.ld), apply the optional GeLU, round to bf16
-// (RNE) or keep fp32, and store.
+// Data path per CTA: TMA (128-byte swizzle) -> shared-memory ring of 128-deep
+// K stages (3 of 64 KiB for 256-wide tiles, 4 of 48 KiB for 128-wide: deep
+// stages, because issuing an MMA, a commit or a TMA copy costs a thread
+// 60-100 cycles, and a 64-deep stage of 4 MMAs holds only 512 tensor
+// cycles of work per SM); the TMA bytes of
+// both CTAs are counted on the even CTA's `full` barrier; one thread of the
+// even CTA issues the MMAs and releases a stage in both CTAs with a multicast
+// commit; the epilogue warps of each CTA read its own TMEM (tcgen05.ld),
+// apply the optional GeLU, round to bf16 (RNE) or keep fp32, and write
+// through swizzled shared-memory boxes and TMA stores.
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner (and
 // MMA issuer in the even CTA), warps 2..9 = epilogue (warp w reads TMEM lanes
-// 32*(w%4)..+31; warps 2..5 take the first 128 accumulator columns, warps
-// 6..9 the last 128).
+// 32*(w%4)..+31; warps 2..5 take the first half of the accumulator columns,
+// warps 6..9 the second half).
 //
-// Two kernels:
-//   gemm_persistent_kernel  one pair per two SMs walks work units (tile,
-//       k-group); the accumulator is double-buffered in TMEM (2 x 256
+// The tile width is a per-unit run-time value no larger than the ring's
+// template width, so one kernel can mix 256- and 128-wide tiles.
+//
+// Kernels:
+//   gemm_persistent_kernel<MAXBN>  one pair per two SMs walks work units
+//       (tile, k-group); the accumulator is double-buffered in TMEM (2 x 256
 //       columns) so the epilogue of one tile overlaps the main loop of the
 //       next.  k-group g selects shard g's K range through the 3-D tensor
-//       maps and its output goes to out + g * out_group_stride (per-shard
+//       maps and its output goes to group g of the output (per-shard
 //       partials); with one k-group the K loop walks shard 0's rows, then
 //       shard 1's, ..., so the row-parallel partial sums are added inside the
 //       accumulator.
-//   gemm_cluster_sum_kernel  for outputs with too few tiles to fill the GPU:
-//       the S pairs of a cluster share one output tile, pair p accumulates
-//       the p-th contiguous slice of the K blocks (with K/n a multiple of the
-//       block depth and S dividing n, slice p is exactly shard group p).  The
-//       S CTAs holding the same 128 rows (one per pair) split them: CTA of
-//       pair p owns rows [p*128/S, (p+1)*128/S) of that half.  Once every
-//       main loop of the cluster is done (a cluster barrier: from then on no
-//       ring is in use), every CTA stores the fp32 partial rows it holds into
-//       slot `its pair` of the owner's shared memory (distributed shared
-//       memory stores), and after a second barrier each owner adds its S
-//       slots in ascending slice order.  The sum never touches HBM.
+//   gemm_cluster_sum_kernel  256-wide tiles for outputs with too few tiles to
+//       fill the GPU: the S pairs of a cluster share one output tile, pair p
+//       accumulates the p-th contiguous slice of the K blocks (with K/n a
+//       multiple of the block depth and S dividing n, slice p is exactly
+//       shard group p).  The S CTAs holding the same 128 rows (one per pair)
+//       split them: CTA of pair p owns rows [p*128/S, (p+1)*128/S) of that
+//       half.  Once every main loop of the cluster is done (a cluster
+//       barrier: from then on no ring is in use), every CTA stores the fp32
+//       partial rows it holds into slot `its pair` of the owner's shared
+//       memory (distributed shared memory stores), and after a second
+//       barrier each owner adds its S slots in ascending slice order.  The
+//       sum never touches HBM.
 #pragma once
 
 #include "tp_device.cuh"
@@ -53,35 +61,43 @@ namespace tpk {
 
 constexpr int BM = 128;              // accumulator rows held by one CTA
 constexpr int PAIR_M = 2 * BM;       // rows of a pair tile
-constexpr int BN = 256;              // columns of a tile (accumulator width)
-constexpr int BN_HALF = BN / 2;      // B columns one CTA stages
-constexpr int BK = 64;               // one 128-byte swizzle row of bf16
+constexpr int MAX_BN = 256;          // widest tile (accumulator columns)
+constexpr int BK = 128;              // K depth of one ring stage
+constexpr int BK_BOX = 64;           // K depth of one A box: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-#ifndef TP_STAGES
-#define TP_STAGES 6
-#endif
-constexpr int STAGES = TP_STAGES;
-constexpr int A_STAGE_BYTES = BM * BK * 2;          // 16 KiB
+constexpr int A_BOX_BYTES = BM * BK_BOX * 2;        // 16 KiB
+constexpr int A_STAGE_BYTES = (BK / BK_BOX) * A_BOX_BYTES;  // 32 KiB
 constexpr int B_CHUNK_N = 64;                       // N columns per TMA box (128 bytes)
-constexpr int B_CHUNK_BYTES = BK * B_CHUNK_N * 2;   // 8 KiB
-constexpr int B_STAGE_BYTES = BK * BN_HALF * 2;     // 16 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr uint32_t PAIR_STAGE_TX = 2 * STAGE_BYTES; // bytes both CTAs land per stage
-#ifndef TP_EPI_WARPS
-#define TP_EPI_WARPS 8
-#endif
-// Epilogue warps: a multiple of 4 (each TMEM lane quadrant is read by
-// EPI_WARPS/4 warps, each taking an equal share of the columns).
-constexpr int EPI_WARPS = TP_EPI_WARPS;
-constexpr int EPI_COL_CHUNKS = BN / 32 / (EPI_WARPS / 4);  // 32-column chunks per epilogue warp
+constexpr int B_CHUNK_BYTES = BK * B_CHUNK_N * 2;   // 16 KiB: 64 columns x 128 k-rows
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quadrant, each half of the columns
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int RED_LD = BN + 4;  // fp32 row pitch of the parked partial tile (bank spread)
 constexpr int STG_BYTES = 32 * 128;  // one epilogue warp's store box: 32 rows x 128 bytes
-static_assert(BM * RED_LD * 4 <= STAGES * STAGE_BYTES, "partial tile must fit in the ring");
+constexpr int ACC_STRIDE = MAX_BN;   // TMEM columns between the two accumulators
+constexpr uint32_t TMEM_COLS_PERSISTENT = 2 * ACC_STRIDE;
+#ifndef TP_RING_KB
+#define TP_RING_KB 192
+#endif
+constexpr int RING_BUDGET = TP_RING_KB * 1024;  // shared memory for the operand ring
+constexpr int MAX_STAGES = 8;
 
-constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, true);
+// Shared-memory ring for tiles up to MAXBN columns: ring | EPI_WARPS store
+// boxes (1024-byte aligned, for the 128-byte swizzle) | barriers.
+template <int MAXBN>
+struct Ring {
+    static constexpr int B_STAGE_BYTES = BK * (MAXBN / 2) * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int STAGES = RING_BUDGET / STAGE_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_WARPS * STG_BYTES + 1024 + 256;
+    static_assert(STAGES <= MAX_STAGES, "barrier array");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
 
-// A descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+constexpr int RED_LD = MAX_BN + 4;  // fp32 row pitch of the parked partial tile (bank spread)
+static_assert(BM * RED_LD * 4 <= Ring<256>::RING_BYTES, "partial tile must fit in the ring");
+
+// A descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart;
+// a stage holds two such boxes (K 0..63 and 64..127), 16 KiB apart.
 // B descriptor: MN-major, 128-byte swizzle; a 64-column chunk holds all BK
 // k-rows (BK * 128 bytes), 8-k-row groups 1024 bytes apart.
 constexpr uint32_t A_SBO = 1024;
@@ -89,27 +105,27 @@ constexpr uint32_t B_LBO = B_CHUNK_BYTES;
 constexpr uint32_t B_SBO = 1024;
 
 struct SmemBarriers {
-    uint64_t full[STAGES];     // even CTA: TMA bytes of both CTAs of the pair
-    uint64_t empty[STAGES];    // both CTAs: stage consumed (multicast commit)
-    uint64_t acc_full[2];      // both CTAs: accumulator ready (multicast commit)
-    uint64_t acc_empty[2];     // even CTA: epilogue warps of both CTAs done
+    uint64_t full[MAX_STAGES];   // even CTA: TMA bytes of both CTAs of the pair
+    uint64_t empty[MAX_STAGES];  // both CTAs: stage consumed (multicast commit)
+    uint64_t acc_full[2];        // both CTAs: accumulator ready (multicast commit)
+    uint64_t acc_empty[2];       // even CTA: epilogue warps of both CTAs done
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
 };
-
-// Shared memory: ring | EPI_WARPS store boxes (1024-byte aligned, for the
-// 128-byte swizzle) | barriers.
-constexpr int GEMM_SMEM_BYTES =
-    STAGES * STAGE_BYTES + EPI_WARPS * STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(sizeof(SmemBarriers) <= 256, "barrier block");
+
+// Bytes both CTAs of a pair land per k-block of a bn-wide tile.
+__host__ __device__ constexpr uint32_t pair_stage_tx(int bn) {
+    return 2u * static_cast<uint32_t>(A_STAGE_BYTES + BK * (bn / 2) * 2);
+}
 
 struct GemmArgs {
     int M, N;
+    int bn;              // tile width: 256 or 128
     int k_blocks;        // BK-deep blocks per k-group (ceil)
     int k_groups;        // 1, or the shard count for per-shard partial outputs
-    int m_tiles, n_tiles;  // pair tiles (PAIR_M x BN)
+    int m_tiles, n_tiles;  // pair tiles (PAIR_M x bn)
     int num_units;       // m_tiles * n_tiles * k_groups (persistent kernel)
     int split;           // pairs per cluster S (cluster kernel)
     void *out;           // [M, N] row-major
@@ -126,8 +142,8 @@ struct GemmArgs {
 };
 
 // ---------------------------------------------------------------------------
-// Epilogue: activation, rounding and store of 8 consecutive columns of one
-// output row (row < M, col < N, col a multiple of 8).  Writes the plain
+// Direct stores: activation, rounding and store of 8 consecutive columns of
+// one output row (row < M, col < N, col a multiple of 8).  Writes the plain
 // output (k-group g) and, if requested, the shard-major copy.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void store_vec8(const GemmArgs &a, int g, int row, int col,
@@ -193,18 +209,18 @@ __device__ __forceinline__ void release_accumulator(uint32_t acc_empty_addr) {
     if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(acc_empty_addr);
 }
 
-// Direct epilogue (per-thread 16-byte stores, one row per lane): used when
-// a shard-major copy is requested.  Columns [c0*32, c0*32 + 32*EPI_COL_CHUNKS)
-// of the accumulator at taddr.
+// Direct epilogue (per-thread 16-byte stores, one row per lane): used when a
+// shard-major copy is requested.  `ncols` accumulator columns starting at
+// column `cofs` of the accumulator at taddr, output columns col_base + cofs...
 __device__ __forceinline__ void epilogue_direct(const GemmArgs &a, uint32_t taddr, int row,
-                                                int col_base, int c0, int g,
+                                                int col_base, int cofs, int ncols, int g,
                                                 uint32_t acc_empty_addr) {
 #pragma unroll 1
-    for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
+    for (int c = 0; c < ncols; c += 32) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_32x32b_x32(taddr + cofs + c, r);
         tmem_ld_wait();
-        store_row_chunk32(a, g, row, col_base + c * 32, r);
+        store_row_chunk32(a, g, row, col_base + cofs + c, r);
     }
     release_accumulator(acc_empty_addr);
 }
@@ -232,25 +248,25 @@ __device__ __forceinline__ void stage_and_store_box(const CUtensorMap *tmC, uint
     }
 }
 
-// TMA-store epilogue: the warp's 32 rows (starting at `row0`) and 128
+// TMA-store epilogue: the warp's 32 rows (starting at `row0`) and `ncols`
 // accumulator columns (starting at `cofs` within the tile at `col_base`).
-// bf16 output: two 64-column boxes; fp32 output: four 32-column boxes.  The
+// bf16 output: 64-column boxes; fp32 output: 32-column boxes.  The
 // accumulator is released as soon as its last tensor-memory load is done.
 // Rows >= M and columns >= N of a box are clipped by the TMA unit.
-__device__ __forceinline__ void epilogue_tma_store(const GemmArgs &a, const CUtensorMap *tmC,
+__device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool out_f32, bool gelu,
                                                    uint32_t taddr, uint32_t stg, int row0,
-                                                   int col_base, int cofs, int g,
+                                                   int col_base, int cofs, int ncols, int g,
                                                    uint32_t acc_empty_addr) {
-    if (!a.out_f32) {
+    if (!out_f32) {
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        for (int c = 0; c < ncols; c += 64) {
             uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(taddr + cofs + j * 64, r0);
-            tmem_ld_32x32b_x32(taddr + cofs + j * 64 + 32, r1);
+            tmem_ld_32x32b_x32(taddr + cofs + c, r0);
+            tmem_ld_32x32b_x32(taddr + cofs + c + 32, r1);
             tmem_ld_wait();
-            if (j == 1) release_accumulator(acc_empty_addr);
+            if (c + 64 >= ncols) release_accumulator(acc_empty_addr);
             uint32_t pk[32];
-            if (a.act_gelu) {
+            if (gelu) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     pk[i] = pack_bf16x2(gelu_f32(__uint_as_float(r0[2 * i])),
@@ -266,20 +282,20 @@ __device__ __forceinline__ void epilogue_tma_store(const GemmArgs &a, const CUte
                         pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
                 }
             }
-            stage_and_store_box(tmC, stg, pk, col_base + cofs + j * 64, row0, g);
+            stage_and_store_box(tmC, stg, pk, col_base + cofs + c, row0, g);
         }
     } else {
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+        for (int c = 0; c < ncols; c += 32) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + cofs + j * 32, r);
+            tmem_ld_32x32b_x32(taddr + cofs + c, r);
             tmem_ld_wait();
-            if (j == 3) release_accumulator(acc_empty_addr);
-            if (a.act_gelu) {
+            if (c + 32 >= ncols) release_accumulator(acc_empty_addr);
+            if (gelu) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gelu_f32(__uint_as_float(r[i])));
             }
-            stage_and_store_box(tmC, stg, r, col_base + cofs + j * 32, row0, g);
+            stage_and_store_box(tmC, stg, r, col_base + cofs + c, row0, g);
         }
     }
 }
@@ -303,31 +319,37 @@ __device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_til
 struct ProducerState {
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t issued = 0;  // loads issued whose stage was not yet seen released
+    uint32_t issued = 0;  // 1 once any load was issued
 };
 
+template <int MAXBN>
 __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                                 uint8_t *ring, SmemBarriers *bars,
                                                 uint32_t full_remote, bool leader, int half,
-                                                ProducerState &ps, int m_tile, int n_tile, int g,
-                                                int kb0, int kb1, uint64_t limit) {
+                                                ProducerState &ps, int m_tile, int n_tile, int bn,
+                                                int g, int kb0, int kb1, uint64_t limit) {
+    using R = Ring<MAXBN>;
     const int row0 = m_tile * PAIR_M + half * BM;
-    const int col0 = n_tile * BN + half * BN_HALF;
+    const int col0 = n_tile * bn + half * (bn / 2);
+    const int chunks = bn / 2 / B_CHUNK_N;
+    const uint32_t tx = pair_stage_tx(bn);
     for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&bars->empty[ps.stage]), ps.phase ^ 1u, limit,
                                &bars->abort, SITE_PRODUCER_EMPTY))
             return false;
-        if (leader) mbar_arrive_expect_tx(smem_u32(&bars->full[ps.stage]), PAIR_STAGE_TX);
+        if (leader) mbar_arrive_expect_tx(smem_u32(&bars->full[ps.stage]), tx);
         const uint32_t fb = full_remote + ps.stage * 8;
-        uint8_t *sa = ring + ps.stage * STAGE_BYTES;
+        uint8_t *sa = ring + ps.stage * R::STAGE_BYTES;
         uint8_t *sb = sa + A_STAGE_BYTES;
-        tma_load_3d_pair(smem_u32(sa), tmA, fb, kb * BK, g, row0);
 #pragma unroll
-        for (int j = 0; j < BN_HALF / B_CHUNK_N; ++j)
+        for (int j = 0; j < BK / BK_BOX; ++j)
+            tma_load_3d_pair(smem_u32(sa + j * A_BOX_BYTES), tmA, fb, kb * BK + j * BK_BOX, g,
+                             row0);
+        for (int j = 0; j < chunks; ++j)
             tma_load_3d_pair(smem_u32(sb + j * B_CHUNK_BYTES), tmB, fb, col0 + j * B_CHUNK_N,
                              kb * BK, g);
         ps.issued = 1;
-        if (++ps.stage == STAGES) {
+        if (++ps.stage == R::STAGES) {
             ps.stage = 0;
             ps.phase ^= 1u;
         }
@@ -338,13 +360,14 @@ __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CU
 // After the last load: wait until every stage of this CTA's ring has been
 // released by the MMA issuer.  The releases are multicast commits from the
 // even CTA; none may still be on its way when the CTA exits.
+template <int MAXBN>
 __device__ __forceinline__ bool producer_tail(SmemBarriers *bars, ProducerState &ps,
                                               uint64_t limit) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < Ring<MAXBN>::STAGES; ++i) {
         if (!mbar_wait_bounded(smem_u32(&bars->empty[ps.stage]), ps.phase ^ 1u, limit,
                                &bars->abort, SITE_PRODUCER_EMPTY))
             return false;
-        if (++ps.stage == STAGES) {
+        if (++ps.stage == Ring<MAXBN>::STAGES) {
             ps.stage = 0;
             ps.phase ^= 1u;
         }
@@ -362,28 +385,39 @@ __device__ __forceinline__ void producer_drain(const ProducerState &ps) {
     }
 }
 
-// MMA issuer (even CTA): accumulate k-blocks [kb0, kb1) into TMEM columns at
-// d_tmem of both CTAs; each consumed stage is released in both CTAs.
+// MMA issuer (even CTA): accumulate k-blocks [kb0, kb1) of a bn-wide tile
+// into TMEM columns at d_tmem of both CTAs; each consumed stage is released
+// in both CTAs.  The shared-memory descriptors are formed once: the start
+// address field (bits 0-13, address >> 4) of a stage's descriptor is the
+// ring's plus stage * STAGE_BYTES / 16; a 16-deep K step adds 32 bytes (2)
+// inside A's swizzle row (the second A box starts 16 KiB, 1024, further) or
+// two 8-row groups (2048 bytes, 128) of B.  Shared addresses stay below
+// 2^18, so no add carries out of the field.
+// The operands arrive through the async proxy (TMA) and are read through it
+// (tcgen05.mma), so the full-barrier wait alone orders them; no tcgen05
+// fence is needed per k-block.
+template <int MAXBN>
 __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, int &stage,
-                                            uint32_t &phase, uint32_t d_tmem, uint16_t pair_mask,
-                                            int kb0, int kb1, uint64_t limit) {
+                                            uint32_t &phase, uint32_t d_tmem, uint32_t idesc,
+                                            uint16_t pair_mask, int kb0, int kb1,
+                                            uint64_t limit) {
+    using R = Ring<MAXBN>;
+    const uint64_t a_ring = smem_desc_sw128(smem_u32(ring), 16, A_SBO);
+    const uint64_t b_ring = smem_desc_sw128(smem_u32(ring) + A_STAGE_BYTES, B_LBO, B_SBO);
     for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, limit, &bars->abort,
                                SITE_MMA_FULL))
             return false;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(ring + stage * STAGE_BYTES);
-        const uint32_t sb = sa + A_STAGE_BYTES;
+        const uint64_t so = static_cast<uint64_t>(stage * (R::STAGE_BYTES >> 4));
+        const uint64_t da = a_ring + so, db = b_ring + so;
+        constexpr int KPB = BK_BOX / UMMA_K;  // K steps per A box
+        umma_f16_pair(d_tmem, da, db, idesc, kb > kb0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k) {
-            // A: advance 16 bf16 (32 bytes) along K inside the swizzle row.
-            // B: advance 16 k-rows = two 8-row groups of 1024 bytes.
-            const uint64_t da = smem_desc_sw128(sa + k * (UMMA_K * 2), 16, A_SBO);
-            const uint64_t db = smem_desc_sw128(sb + k * (UMMA_K / 8) * B_SBO, B_LBO, B_SBO);
-            umma_f16_pair(d_tmem, da, db, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 1; k < BK / UMMA_K; ++k)
+            umma_f16_pair(d_tmem, da + (A_BOX_BYTES >> 4) * (k / KPB) + 2 * (k % KPB),
+                          db + 128 * k, idesc, 1u);
         umma_commit_pair_mc(smem_u32(&bars->empty[stage]), pair_mask);
-        if (++stage == STAGES) {
+        if (++stage == R::STAGES) {
             stage = 0;
             phase ^= 1u;
         }
@@ -405,12 +439,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // the peer has initialised it.  Then the programmatic-launch hand-off: the
 // next kernel of the stream may start launching, and this one waits for the
 // previous kernel to complete.
-__device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_cols,
-                                           const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                           const CUtensorMap *tmC, bool store_map) {
+__device__ __forceinline__ void gemm_setup(SmemBarriers *bars, int stages, uint32_t tmem_cols,
+                                           const CUtensorMap *const *maps, int nmaps) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
@@ -424,9 +457,7 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, uint32_t tmem_col
         fence_proxy_async_smem();
     }
     if (warp == 0 && (threadIdx.x & 31) == 0) {
-        tma_prefetch_desc(tmA);
-        tma_prefetch_desc(tmB);
-        if (store_map) tma_prefetch_desc(tmC);
+        for (int i = 0; i < nmaps; ++i) tma_prefetch_desc(maps[i]);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(&bars->tmem_base), tmem_cols);
@@ -454,24 +485,27 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, uint32_t tmem_
 // ---------------------------------------------------------------------------
 // Persistent kernel: cluster = one pair, grid = 2 x (pairs launched).
 // ---------------------------------------------------------------------------
+template <int MAXBN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
+    using R = Ring<MAXBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
-    uint8_t *staging = ring + STAGES * STAGE_BYTES;
+    uint8_t *staging = ring + R::RING_BYTES;
     SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(staging + EPI_WARPS * STG_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t TMEM_COLS = 2 * BN;
 
     const int half = static_cast<int>(cluster_ctarank());  // 0 = even (leader), 1 = odd
     const bool leader = half == 0;
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
+    const int bn = a.bn;
 
-    gemm_setup(bars, TMEM_COLS, &tmA, &tmB, &tmC, a.tma_store != 0);
+    const CUtensorMap *maps[3] = {&tmA, &tmB, &tmC};
+    gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps, a.tma_store ? 3 : 2);
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
@@ -483,15 +517,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int u = pair; u < a.num_units && ok; u += num_pairs) {
                 int mt, nt, g;
                 decode_unit(a, u, mt, nt, g);
-                ok = produce_kblocks(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt,
-                                     nt, g, 0, a.k_blocks, limit);
+                ok = produce_kblocks<MAXBN>(&tmA, &tmB, ring, bars, full_remote, leader, half, ps,
+                                            mt, nt, bn, g, 0, a.k_blocks, limit);
             }
-            if (ok) ok = producer_tail(bars, ps, limit);
+            if (ok) ok = producer_tail<MAXBN>(bars, ps, limit);
             if (!ok) producer_drain(ps);
         }
         __syncwarp();
     } else if (warp == 1) {
         if (leader && lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(PAIR_M, bn, true);
             int stage = 0, local = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -502,8 +537,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                        &bars->abort, SITE_MMA_ACC_EMPTY);
                 if (!ok) break;
                 tc_fence_after();
-                ok = mma_kblocks(ring, bars, stage, phase, tmem_base + acc * BN, 0x3, 0,
-                                 a.k_blocks, limit);
+                ok = mma_kblocks<MAXBN>(ring, bars, stage, phase, tmem_base + acc * ACC_STRIDE,
+                                        idesc, 0x3, 0, a.k_blocks, limit);
                 if (!ok) break;
                 umma_commit_pair_mc(smem_u32(&bars->acc_full[acc]), 0x3);
             }
@@ -511,8 +546,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;                             // TMEM lane quadrant
-        const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;  // first 32-column chunk
+        const int q = warp & 3;                         // TMEM lane quadrant
+        const int cofs = ((warp - 2) >> 2) * (bn / 2);  // this warp's half of the columns
         const uint32_t acc_empty_remote = dsmem_map(smem_u32(&bars->acc_empty[0]), 0);
         const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
         int local = 0;
@@ -525,33 +560,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             int mt, nt, g;
             decode_unit(a, u, mt, nt, g);
-            const uint32_t taddr = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t taddr =
+                tmem_base + acc * ACC_STRIDE + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t release = acc_empty_remote + acc * 8;
+            const int row0 = mt * PAIR_M + half * BM + q * 32;
             if (a.tma_store)
-                epilogue_tma_store(a, &tmC, taddr, stg, mt * PAIR_M + half * BM + q * 32,
-                                   nt * BN, c0 * 32, g, release);
+                epilogue_tma_store(&tmC, a.out_f32 != 0, a.act_gelu != 0, taddr, stg, row0,
+                                   nt * bn, cofs, bn / 2, g, release);
             else
-                epilogue_direct(a, taddr, mt * PAIR_M + half * BM + q * 32 + lane, nt * BN, c0,
-                                g, release);
+                epilogue_direct(a, taddr, row0 + lane, nt * bn, cofs, bn / 2, g, release);
         }
         if (lane == 0) bulk_wait0();  // every store box has left shared memory and landed
         __syncwarp();
     }
 
-    gemm_teardown(tmem_base, TMEM_COLS);
+    gemm_teardown(tmem_base, TMEM_COLS_PERSISTENT);
 }
 
 // ---------------------------------------------------------------------------
-// Cluster split kernel: grid = 2 * S * tiles CTAs, cluster = 2 * S CTAs along
-// x (S pairs; cluster rank 2p + h is half h of pair p).
+// Cluster split kernel (256-wide tiles): grid = 2 * S * tiles CTAs, cluster =
+// 2 * S CTAs along x (S pairs; cluster rank 2p + h is half h of pair p).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_cluster_sum_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
+    using R = Ring<256>;
+    constexpr int BN = 256;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
-    uint8_t *staging = ring + STAGES * STAGE_BYTES;
+    uint8_t *staging = ring + R::RING_BYTES;
     SmemBarriers *bars = reinterpret_cast<SmemBarriers *>(staging + EPI_WARPS * STG_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -568,7 +606,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int kb0 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * p) / S);
     const int kb1 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * (p + 1)) / S);
 
-    gemm_setup(bars, TMEM_COLS, &tmA, &tmB, &tmC, a.tma_store != 0);
+    const CUtensorMap *maps[2] = {&tmA, &tmB};
+    gemm_setup(bars, R::STAGES, TMEM_COLS, maps, 2);
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
     float *red = reinterpret_cast<float *>(ring);  // parks the fp32 partial tile
@@ -579,9 +618,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t full_remote =
                 dsmem_map(smem_u32(&bars->full[0]), static_cast<uint32_t>(2 * p));
             ProducerState ps;
-            if (!produce_kblocks(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt, nt, 0,
-                                 kb0, kb1, limit) ||
-                !producer_tail(bars, ps, limit))
+            if (!produce_kblocks<256>(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt,
+                                      nt, BN, 0, kb0, kb1, limit) ||
+                !producer_tail<256>(bars, ps, limit))
                 producer_drain(ps);
         }
         __syncwarp();
@@ -589,7 +628,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (leader && lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            if (mma_kblocks(ring, bars, stage, phase, tmem_base, pair_mask, kb0, kb1, limit))
+            if (mma_kblocks<256>(ring, bars, stage, phase, tmem_base,
+                                 idesc_bf16_f32(PAIR_M, BN, true), pair_mask, kb0, kb1, limit))
                 umma_commit_pair_mc(smem_u32(&bars->acc_full[0]), pair_mask);
             else
                 mma_drain(bars, limit);
@@ -612,7 +652,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // rit / (BM/S).
         fence_proxy_async_smem();
         const int q = warp & 3;
-        const int c0 = ((warp - 2) >> 2) * EPI_COL_CHUNKS;
+        const int cofs = ((warp - 2) >> 2) * (BN / 2);
         const int rows_per = BM / S;
         const int rit = q * 32 + lane;
         const int owner_p = rit / rows_per;
@@ -621,16 +661,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         float *dst = red + slot_row * RED_LD;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-        for (int c = c0; c < c0 + EPI_COL_CHUNKS; ++c) {
+        for (int c = cofs; c < cofs + BN / 2; c += 32) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_32x32b_x32(taddr + c, r);
             tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 const float4 val =
                     make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
                                 __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
-                float *ptr = dst + c * 32 + v * 4;
+                float *ptr = dst + c + v * 4;
                 if (owner == rank)
                     *reinterpret_cast<float4 *>(ptr) = val;
                 else

@@ -73,6 +73,126 @@ __global__ void __launch_bounds__(256) shard_reduce_kernel(const float *__restri
     }
 }
 
+// Streaming reduce through shared memory: a persistent kernel, one CTA per
+// SM.  The output is cut into chunks of `chunk` elements (a multiple of 8);
+// CTA b takes chunks b, b + grid, ...  For each chunk one thread issues one
+// bulk copy per shard (chunk * 4 contiguous bytes of P_i) into a stage of a
+// RED_STAGES-deep ring in shared memory, all counted on the stage's `full`
+// barrier; the 256 consumer threads add the shards of 8 consecutive
+// elements in ascending shard order in fp32 from shared memory and store 16
+// bytes of bf16 (or 32 of fp32), and each consumer warp releases the stage.
+// Large contiguous copies keep every DRAM page open for long runs, and the
+// copies are issued by one thread, so no register file holds data in flight.
+constexpr int RED_STAGES = 3;
+constexpr int RED_STAGE_BYTES = 64 * 1024;
+constexpr int RED_CONSUMERS = 256;
+constexpr int RED_THREADS = 32 + RED_CONSUMERS;
+constexpr int RED_SMEM_BYTES = RED_STAGES * RED_STAGE_BYTES + 128;
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(RED_THREADS, 1)
+    shard_reduce_bulk_kernel(const float *__restrict__ P, void *__restrict__ Y, int64_t total,
+                             int n_shards, int chunk, uint64_t limit_ns) {
+    extern __shared__ __align__(128) uint8_t red_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(red_smem + RED_STAGES * RED_STAGE_BYTES);
+    uint64_t *empty = full + RED_STAGES;
+    uint32_t *abort = reinterpret_cast<uint32_t *>(empty + RED_STAGES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RED_STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), RED_CONSUMERS / 32);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
+
+    const int64_t n_chunks = (total + chunk - 1) / chunk;
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool issued = false, ok = true;
+            for (int64_t c = blockIdx.x; c < n_chunks && ok; c += gridDim.x) {
+                if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, limit_ns, abort,
+                                       SITE_PRODUCER_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const int64_t e0 = c * chunk;
+                const int64_t n = total - e0 < chunk ? total - e0 : chunk;
+                const uint32_t bytes = static_cast<uint32_t>(n * 4);
+                const uint32_t fb = smem_u32(&full[stage]);
+                mbar_arrive_expect_tx(fb, bytes * static_cast<uint32_t>(n_shards));
+                const uint32_t dst = smem_u32(red_smem + stage * RED_STAGE_BYTES);
+                for (int i = 0; i < n_shards; ++i)
+                    bulk_load(dst + static_cast<uint32_t>(i) * static_cast<uint32_t>(chunk) * 4u,
+                              P + static_cast<int64_t>(i) * total + e0, bytes, fb);
+                issued = true;
+                if (++stage == RED_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // every stage released before exit (a copy still landing after
+            // an abort is waited for the same way, with the drain limit)
+            for (int s = 0; s < RED_STAGES && issued; ++s) {
+                if (ok) {
+                    ok = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, limit_ns, abort,
+                                           SITE_PRODUCER_EMPTY);
+                } else {
+                    mbar_wait_drain(smem_u32(&full[stage]), phase ^ 1u, limit_ns);
+                }
+                if (++stage == RED_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        const int t = threadIdx.x - 32;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+            if (!mbar_wait_warp(smem_u32(&full[stage]), phase, limit_ns, abort, SITE_MMA_FULL))
+                break;
+            const int64_t e0 = c * chunk;
+            const int n = static_cast<int>(total - e0 < chunk ? total - e0 : chunk);
+            const float *src = reinterpret_cast<const float *>(red_smem + stage * RED_STAGE_BYTES);
+            for (int e = t * 8; e < n; e += RED_CONSUMERS * 8) {
+                float4 a0 = *reinterpret_cast<const float4 *>(src + e);
+                float4 a1 = *reinterpret_cast<const float4 *>(src + e + 4);
+                for (int i = 1; i < n_shards; ++i) {
+                    const float *q = src + static_cast<int64_t>(i) * chunk + e;
+                    add4(a0, *reinterpret_cast<const float4 *>(q));
+                    add4(a1, *reinterpret_cast<const float4 *>(q + 4));
+                }
+                if constexpr (OUT_BF16) {
+                    const uint4 u = make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
+                                               pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
+                    __stcs(reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(Y) + e0 + e), u);
+                } else {
+                    float4 *y = reinterpret_cast<float4 *>(static_cast<float *>(Y) + e0 + e);
+                    __stcs(y, a0);
+                    __stcs(y + 1, a1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+            if (++stage == RED_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    __syncthreads();
+}
+
 // Element-wise fallback for sizes that are not a multiple of 8 elements:
 // same ascending-order fp32 sum, one element per thread.
 template <bool OUT_BF16>

@@ -32,11 +32,11 @@ struct DeviceInfo {
 
 // How many clusters of `size` GEMM CTAs can be resident at once (0 if the
 // size cannot be launched).
-int active_clusters(const void *kernel, int size) {
+int active_clusters(const void *kernel, int size, int smem_bytes) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(size), 1, 1);
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(size);
@@ -63,18 +63,32 @@ tp_status device_info(DeviceInfo **out) {
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return TP_ERR_CUDA;
-        if (cudaFuncSetAttribute(gemm_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES) != cudaSuccess)
-            return TP_ERR_CUDA;
-        if (cudaFuncSetAttribute(gemm_cluster_sum_kernel,
+        if (cudaFuncSetAttribute(gemm_persistent_kernel<256>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_BYTES) != cudaSuccess)
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<128>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_cluster_sum_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(shard_reduce_bulk_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 RED_SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(shard_reduce_bulk_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 RED_SMEM_BYTES) != cudaSuccess)
             return TP_ERR_CUDA;
-        d.max_pairs = active_clusters(reinterpret_cast<const void *>(gemm_persistent_kernel), 2);
+        d.max_pairs = active_clusters(reinterpret_cast<const void *>(gemm_persistent_kernel<256>),
+                                      2, Ring<256>::SMEM_BYTES);
+        const int p128 = active_clusters(
+            reinterpret_cast<const void *>(gemm_persistent_kernel<128>), 2, Ring<128>::SMEM_BYTES);
+        if (p128 < d.max_pairs) d.max_pairs = p128;
         if (d.max_pairs < 1) return TP_ERR_CUDA;
         for (int l = 1; l <= 2; ++l)  // S = 2, 4 pairs: clusters of 4 and 8 CTAs
-            d.max_clusters[l] =
-                active_clusters(reinterpret_cast<const void *>(gemm_cluster_sum_kernel), 2 << l);
+            d.max_clusters[l] = active_clusters(
+                reinterpret_cast<const void *>(gemm_cluster_sum_kernel), 2 << l,
+                Ring<256>::SMEM_BYTES);
         d.ready = true;
     }
     *out = &d;
@@ -165,17 +179,69 @@ struct GemmCall {
     bool allow_split;
 };
 
-// Pairs per cluster for outputs with too few pair tiles to occupy the GPU:
-// the largest S in {2, 4} such that tiles * S clusters of 2*S CTAs are all
-// resident at once and each pair gets at least one k-block; 1 means the
-// persistent kernel.
-int choose_split(int tiles, int k_blocks, const DeviceInfo &dev) {
-    int S = 1;
-    for (int l = 1; l <= 2; ++l) {
-        const int s2 = 1 << l;
-        if (tiles <= dev.max_clusters[l] && s2 <= k_blocks) S = s2;
+// Launch plan of one GEMM: tile width and, for the cluster split kernel,
+// pairs per cluster S (S = 1: persistent kernel).
+struct GemmPlan {
+    int bn = 256;
+    int split = 1;
+};
+
+// Optional override of the automatic plan, for measurements:
+// TP_GEMM_PLAN = "256" | "128" | "split2" | "split4".
+// Read at every launch, so that a process can compare plans.
+int plan_override() {
+    const char *e = std::getenv("TP_GEMM_PLAN");
+    if (!e) return 0;
+    if (!std::strcmp(e, "256")) return 1;
+    if (!std::strcmp(e, "128")) return 2;
+    if (!std::strcmp(e, "split2")) return 3;
+    if (!std::strcmp(e, "split4")) return 4;
+    return 0;
+}
+
+// Picks the plan with the smallest estimated time, in units of one k-block
+// of a 256-wide pair tile (128 deep, about 1024 tensor-core cycles):
+//   persistent, width bn: waves * k_blocks * (bn / 256) * overhead(bn) plus
+//       the exposed epilogue of the last tile (larger with GeLU);
+//   split over S pairs (256-wide, one wave of clusters): k_blocks / S plus
+//       the shared-memory reduction of the partial tiles.
+// A 128-wide k-block carries half the tensor work of a 256-wide one but the
+// same issue work (MMA and TMA instructions per stage) and 3/4 of its
+// operand bytes; measured, it takes about 0.75 of the 256-wide time.
+GemmPlan plan_gemm(int64_t M, int64_t N, int k_blocks, int k_groups, bool allow_split, bool gelu,
+                   const DeviceInfo &dev) {
+    const int64_t m_tiles = (M + PAIR_M - 1) / PAIR_M;
+    const int64_t u256 = m_tiles * ((N + 255) / 256) * k_groups;
+    const int64_t u128 = m_tiles * ((N + 127) / 128) * k_groups;
+    const int64_t P = dev.max_pairs;
+    const double tail = gelu ? 6.0 : 2.0;
+    const double c256 = static_cast<double>((u256 + P - 1) / P) * k_blocks + tail;
+    const double c128 = static_cast<double>((u128 + P - 1) / P) * k_blocks * 0.5 * 1.5 + tail / 2;
+    GemmPlan best;
+    double cbest = c256;
+    if (c128 < cbest) {
+        best.bn = 128;
+        cbest = c128;
     }
-    return S;
+    const bool can_split = allow_split && k_groups == 1;
+    for (int l = 1; l <= 2 && can_split; ++l) {
+        const int S = 1 << l;
+        if (u256 > dev.max_clusters[l] || S > k_blocks) continue;
+        const double cs = static_cast<double>(k_blocks) / S + 12.0 + tail;
+        if (cs < cbest) {
+            best.bn = 256;
+            best.split = S;
+            cbest = cs;
+        }
+    }
+    switch (plan_override()) {
+        case 1: return GemmPlan{256, 1};
+        case 2: return GemmPlan{128, 1};
+        case 3: if (can_split && u256 <= dev.max_clusters[1] && k_blocks >= 2) return GemmPlan{256, 2}; break;
+        case 4: if (can_split && u256 <= dev.max_clusters[2] && k_blocks >= 4) return GemmPlan{256, 4}; break;
+        default: break;
+    }
+    return best;
 }
 
 tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
@@ -186,8 +252,9 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     const int64_t Kg = c.K / c.k_groups;
     CUtensorMap tmA, tmB;
     // A viewed as [M][k_groups][Kg]; box = 128 rows x 64 k of one group.
-    if (!encode_3d(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK, 1, BM)) return TP_ERR_CUDA;
-    // B viewed as [k_groups][Kg][N]; box = 64 k-rows x 64 columns of one group.
+    if (!encode_3d(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK_BOX, 1, BM))
+        return TP_ERR_CUDA;
+    // B viewed as [k_groups][Kg][N]; box = 128 k-rows x 64 columns of one group.
     if (!encode_3d(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
         return TP_ERR_CUDA;
 
@@ -209,8 +276,10 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.N = static_cast<int>(c.N);
     a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
     a.k_groups = c.k_groups;
+    const GemmPlan plan = plan_gemm(c.M, c.N, a.k_blocks, c.k_groups, c.allow_split, c.gelu, *dev);
+    a.bn = plan.bn;
     a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
-    a.n_tiles = static_cast<int>((c.N + BN - 1) / BN);
+    a.n_tiles = static_cast<int>((c.N + a.bn - 1) / a.bn);
     a.num_units = a.m_tiles * a.n_tiles * c.k_groups;
     a.out = c.out;
     a.out_group_stride = c.out_group_stride;
@@ -225,14 +294,15 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.wait_limit_ns = wait_limit_ns();
 
     const int tiles = a.m_tiles * a.n_tiles;
-    const int S = (c.allow_split && c.k_groups == 1) ? choose_split(tiles, a.k_blocks, *dev) : 1;
+    const int S = plan.split;
     a.split = S;
     const int pairs = S > 1 ? tiles * S : (a.num_units < dev->max_pairs ? a.num_units
                                                                          : dev->max_pairs);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.dynamicSmemBytes = static_cast<size_t>(a.bn == 128 ? Ring<128>::SMEM_BYTES
+                                                           : Ring<256>::SMEM_BYTES);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -246,9 +316,13 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = S > 1
-                              ? cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, tmC, a)
-                              : cudaLaunchKernelEx(&cfg, gemm_persistent_kernel, tmA, tmB, tmC, a);
+    cudaError_t e;
+    if (S > 1)
+        e = cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, tmC, a);
+    else if (a.bn == 128)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<128>, tmA, tmB, tmC, a);
+    else
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256>, tmA, tmB, tmC, a);
     if (e != cudaSuccess) return TP_ERR_CUDA;
     return launch_status();
 }
@@ -290,6 +364,25 @@ int reduce_grid(int64_t work_items, int sm_count) {
 template <bool BF16>
 tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_count,
                           cudaStream_t s) {
+    if (total % 8 == 0) {
+        // bulk-copy pipeline: each stage holds `chunk` elements of every shard
+        const int chunk = (RED_STAGE_BYTES / (4 * n)) & ~7;
+        const int64_t n_chunks = (total + chunk - 1) / chunk;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(n_chunks < sm_count ? n_chunks : sm_count), 1, 1);
+        cfg.blockDim = dim3(RED_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = RED_SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, shard_reduce_bulk_kernel<BF16>, P, Y, total, n, chunk,
+                               wait_limit_ns()) != cudaSuccess)
+            return TP_ERR_CUDA;
+        return launch_status();
+    }
     if (total % 8 != 0) {
         shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n);
         return launch_status();

@@ -162,6 +162,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Same load for a CTA pair that issues one tcgen05.mma.cta_group::2: the data
 // lands in this CTA's shared memory, the completed bytes are counted on the
 // barrier at `cluster_bar`, which may belong to the peer CTA of the pair.

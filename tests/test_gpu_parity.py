@@ -192,6 +192,46 @@ def test_gelu_epilogue_accuracy(tp, cuda_device):
         f"GeLU({xin.flat[worst]}) = {got.flat[worst]!r}, oracle {ref.flat[worst]!r}")
 
 
+def _with_plan(plan, fn):
+    import os
+    old = os.environ.get("TP_GEMM_PLAN")
+    os.environ["TP_GEMM_PLAN"] = plan
+    try:
+        return fn()
+    finally:
+        if old is None:
+            del os.environ["TP_GEMM_PLAN"]
+        else:
+            os.environ["TP_GEMM_PLAN"] = old
+
+
+@pytest.mark.parametrize("M,K,N,n", [(300, 328, 640, 2), (513, 1024, 392, 4), (1000, 512, 1152, 8)])
+def test_tile_plans_agree(tp, cuda_device, M, K, N, n):
+    """Every launch plan (256- and 128-wide pair tiles, cluster split over 2
+    or 4 pairs) on the same column (GeLU) and row products: the persistent
+    plans accumulate every element in the same order, so their outputs are
+    bit-identical; the split plans add slice partials and are held to the
+    accuracy bar against the oracle."""
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=7 * M + N)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Xd, Wd = oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb)
+    col_ref, _ = oracle.column_linear(Xd, Wd, n, act="gelu")
+    row_ref, _ = oracle.row_linear(Xd, Wd, n)
+    outs = {}
+    for plan in ["256", "128", "split2", "split4"]:
+        Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+        Yr = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+        _with_plan(plan, lambda: tp.tp_column_linear(X, W, Yc, None, n_shards=n, act="gelu"))
+        _with_plan(plan, lambda: tp.tp_row_linear(X, W, Yr, None, n_shards=n))
+        _status_ok(tp)
+        assert_bf16_parity(bf16_dev_to_f64(Yc), col_ref, f"column, plan {plan}")
+        assert_bf16_parity(dev_to_f64(Yr), row_ref, f"row, plan {plan}", out_bf16=False)
+        outs[plan] = (dev_bits(Yc), dev_bits(Yr))
+    np.testing.assert_array_equal(outs["256"][0], outs["128"][0])
+    np.testing.assert_array_equal(outs["256"][1], outs["128"][1])
+
+
 @pytest.mark.parametrize("M,K,G,n,sw", [(256, 128, 3, 4, 64), (130, 64, 3, 2, 8), (64, 32, 2, 8, 16)])
 def test_column_linear_head_groups(tp, cuda_device, M, K, G, n, sw):
     """Head-group split: shard i owns slice i of each of the G column blocks."""
