@@ -285,6 +285,10 @@ def run_ours(args):
         raise RuntimeError("device status error during warm-up")
 
     # ---------------------------------------------------- timed region ----
+    # Every PREQUEUE_BATCH steps a sleep kernel holds the GPU while the host
+    # enqueues the next batch, so that each step's start event is already
+    # followed by its kernels in the queue: the events then bracket device
+    # work only, not host launch latency (which the e2e leg below includes).
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
@@ -294,6 +298,7 @@ def run_ours(args):
     with ClockSampler(dev) as clk:
         t_wall0 = time.perf_counter()
         for i in range(K):
+            _prequeue(torch, i)
             flush.zero_()
             ev[i][0].record(stream)
             step()
@@ -309,6 +314,7 @@ def run_ours(args):
     # per-kernel attribution: the same two GEMM launches with an event between
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     for i in range(K):
+        _prequeue(torch, i)
         flush.zero_()
         ev3[i][0].record(stream)
         tp.tp_column_linear(X, W1, H, None, n_shards=n, act="gelu")
@@ -329,20 +335,8 @@ def run_ours(args):
         cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
 
     # --------------------------------------------------------------- e2e ----
-    Xh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
-    Yh = torch.empty(M, d, dtype=torch.bfloat16).pin_memory()
-    Ke = min(K, 500) if not args.skip_extras else 1
-    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(Ke)]
-    torch.cuda.synchronize()
-    for i in range(Ke):
-        eve[i][0].record(stream)
-        X.copy_(Xh, non_blocking=True)
-        step()
-        Yh.copy_(Y, non_blocking=True)
-        eve[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
+    Ke = min(K, 500) if not args.skip_extras else 3
+    e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
 
     # --------------------------------------------------- max over ranks -----
     dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], dev, world)
@@ -355,7 +349,9 @@ def run_ours(args):
                                    (k2_ms, flops_k2, "gemm row + shard sum (H.W2)"))
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    traffic = _profile_traffic(args.workload)
+    # DRAM bytes per launch of the dominant kernel, from the committed capture
+    traffic = _profile_traffic(args.workload,
+                               "bytes" if dom_name.startswith("gemm row") else "column_gemm_bytes")
 
     if rank != 0:
         if world > 1:
@@ -399,8 +395,11 @@ def run_ours(args):
         "concat": cat,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * d * 2,
-                "ms_per_step": round(e2e_ms, 5),
-                "note": "X copied from pinned host memory, tp_mlp_block, Y copied back"},
+                "ms_per_step": round(e2e_ms, 5), "copy_us_alone": copy_us,
+                "note": "per step: X copied from pinned host memory, tp_mlp_block, Y copied "
+                        "back to pinned host memory; copies on their own streams, double "
+                        "buffered, so step i's copies overlap the neighbouring steps' "
+                        "kernels; timed from the first copy in to the last copy out"},
         "gpu_launches": 2 * K,
         "cpu_baseline": cpu,
         "clocks": clocks,
@@ -409,6 +408,65 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+PREQUEUE_BATCH = 20
+PREQUEUE_SLEEP_CYCLES = 10_000_000  # ~5 ms at 2 GHz, longer than enqueuing a batch
+
+
+def _prequeue(torch, i):
+    if i % PREQUEUE_BATCH == 0:
+        torch.cuda._sleep(PREQUEUE_SLEEP_CYCLES)
+
+
+def run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, K, compute):
+    """End-to-end steps through the public API: copy X in from pinned host
+    memory, tp_mlp_block, copy Y out to pinned host memory.  Copies run on
+    their own streams with two device buffers each way, so consecutive
+    steps overlap; returns (ms per step from the first copy in to the last
+    copy out, {h2d, d2h: microseconds of one copy alone})."""
+    dev = compute.device
+    Xh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Yh = [torch.empty(M, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    Xd = [torch.empty(M, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    Yd = [torch.empty(M, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    mk = lambda: torch.cuda.Event(enable_timing=False)
+    in_done, comp_done, out_done = [mk(), mk()], [mk(), mk()], [mk(), mk()]
+    # one copy alone each way, for the record
+    t = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    t[0].record(compute)
+    Xd[0].copy_(Xh, non_blocking=True)
+    t[1].record(compute)
+    Yh[0].copy_(Yd[0], non_blocking=True)
+    t[2].record(compute)
+    torch.cuda.synchronize()
+    copy_us = {"h2d": round(t[0].elapsed_time(t[1]) * 1e3, 1),
+               "d2h": round(t[1].elapsed_time(t[2]) * 1e3, 1)}
+    for b in range(2):
+        comp_done[b].record(compute)
+        out_done[b].record(compute)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(s_in)
+    for i in range(K):
+        b = i & 1
+        s_in.wait_event(comp_done[b])       # step i-2 no longer reads Xd[b]
+        with torch.cuda.stream(s_in):
+            Xd[b].copy_(Xh, non_blocking=True)
+        in_done[b].record(s_in)
+        compute.wait_event(in_done[b])
+        compute.wait_event(out_done[b])     # step i-2's result has left Yd[b]
+        tp.tp_mlp_block(Xd[b], W1, W2, Yd[b], ws, n_shards=n, stream=compute)
+        comp_done[b].record(compute)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            Yh[b].copy_(Yd[b], non_blocking=True)
+        out_done[b].record(s_out)
+    end.record(s_out)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / K, copy_us
 
 
 def max_over_ranks(values, device, world):
@@ -441,9 +499,9 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def _profile_traffic(workload):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    capture, or None when there is none or the kernels changed since."""
+def _profile_traffic(workload, field="bytes"):
+    """DRAM bytes per launch of a kernel of this workload from the committed
+    ncu capture, or None when there is none or the kernels changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -452,7 +510,7 @@ def _profile_traffic(workload):
         return None
     if not entry or entry.get("source_sha") != kernel_source_sha():
         return None
-    return entry.get("bytes")
+    return entry.get(field)
 
 
 def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
@@ -477,6 +535,7 @@ def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
             "unit": "GB/s", "ms_per_launch": round(ms, 5), "bytes_per_launch": nbytes,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": _profile_traffic(f"reduce_{n}x{rows}x{cols}"),
                          "peak_source": peaks["source"] + " copy bandwidth"},
             "l2": "inputs (1.07 GB) larger than L2"}
 
@@ -505,8 +564,27 @@ def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=
             "bytes_per_launch": nbytes,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": _profile_traffic(f"concat_{n}x{rows}x{sc}_g{groups}"),
                          "peak_source": peaks["source"] + " copy bandwidth"},
             "l2": "flushed before every timed launch"}
+
+
+def run_leg(args):
+    """A few launches of one standalone kernel at its bench workload."""
+    import torch
+    from tensor_sharded_linear_02_b300 import binding as tp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+    K = max(1, args.steps)
+    if args.leg == "reduce":
+        bench_reduce(tp, dev, stream, peaks, K=K)
+    else:
+        bench_concat(tp, dev, stream, peaks, K=K)
+    torch.cuda.synchronize()
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error")
 
 
 # ------------------------------------------------------ reference arm ------
@@ -566,6 +644,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--leg", choices=["reduce", "concat"], default=None,
+                    help="run only a few launches of one standalone kernel at its bench "
+                         "workload and print nothing else (for profiler captures)")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the MLP step (for profiler captures)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -575,6 +656,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.leg:
+        run_leg(args)
     else:
         run_ours(args)
 

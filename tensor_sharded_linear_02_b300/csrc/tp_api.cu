@@ -142,6 +142,61 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A tensor map depends only on its arguments, so encoded maps are kept in a
+// small least-recently-used cache: a call with the buffers and sizes of an
+// earlier one (every step of a model) skips the driver's encoder.  A buffer
+// freed and reallocated at the same address with the same sizes gets the
+// same map, which is the correct one.
+struct MapKey {
+    const void *base;
+    uint64_t dims[3], strides[2];
+    uint32_t box[3];
+    uint32_t f32;
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    uint64_t stamp;
+};
+
+constexpr int kMapCache = 32;
+std::mutex g_map_mutex;
+MapEntry g_maps[kMapCache];
+uint64_t g_map_clock = 0;
+
+bool encode_3d_cached(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+                      uint32_t b2, bool f32 = false) {
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.dims[0] = d0; k.dims[1] = d1; k.dims[2] = d2;
+    k.strides[0] = stride1_bytes; k.strides[1] = stride2_bytes;
+    k.box[0] = b0; k.box[1] = b1; k.box[2] = b2;
+    k.f32 = f32 ? 1u : 0u;
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (MapEntry &e : g_maps) {
+            if (e.stamp != 0 && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+                *m = e.map;
+                e.stamp = ++g_map_clock;
+                return true;
+            }
+        }
+    }
+    if (!encode_3d(m, base, d0, d1, d2, stride1_bytes, stride2_bytes, b0, b1, b2, f32))
+        return false;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    MapEntry *victim = &g_maps[0];
+    for (MapEntry &e : g_maps)
+        if (e.stamp < victim->stamp) victim = &e;
+    victim->key = k;
+    victim->map = *m;
+    victim->stamp = ++g_map_clock;
+    return true;
+}
+
 // ------------------------------------------------------------- validation --
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -252,10 +307,10 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     const int64_t Kg = c.K / c.k_groups;
     CUtensorMap tmA, tmB;
     // A viewed as [M][k_groups][Kg]; box = 128 rows x 64 k of one group.
-    if (!encode_3d(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK_BOX, 1, BM))
+    if (!encode_3d_cached(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK_BOX, 1, BM))
         return TP_ERR_CUDA;
     // B viewed as [k_groups][Kg][N]; box = 128 k-rows x 64 columns of one group.
-    if (!encode_3d(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
+    if (!encode_3d_cached(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
         return TP_ERR_CUDA;
 
     // Output viewed as [k_groups][M][N]; box = 32 rows x 128 bytes of one group.
@@ -264,7 +319,7 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     std::memset(&tmC, 0, sizeof(tmC));
     if (tma_store) {
         const uint64_t es = c.out_f32 ? 4 : 2;
-        if (!encode_3d(&tmC, c.out, c.N, c.M, c.k_groups, c.N * es,
+        if (!encode_3d_cached(&tmC, c.out, c.N, c.M, c.k_groups, c.N * es,
                        (c.k_groups > 1 ? c.out_group_stride : c.M * c.N) * es,
                        static_cast<uint32_t>(128 / es), 32, 1, c.out_f32))
             return TP_ERR_CUDA;
