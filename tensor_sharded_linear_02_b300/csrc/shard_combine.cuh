@@ -4,73 +4,21 @@
 //   shard_reduce  Y[r, c] = sum_i P[i, r, c]   (all-reduce -> on-device sum)
 //   shard_concat  Y[:, cols of shard i] = Ys[i] (all-gather -> on-device concat)
 //
-// Both stream 16-byte vectors with fully coalesced loads and stores; the grid
-// is a whole number of waves over the SMs and each thread walks a grid
-// stride.  Partials are read with the streaming (evict-first) hint since
-// every byte is touched exactly once.
+// Both stream through a shared-memory ring filled by bulk/TMA copies issued
+// by one thread per SM: the reduce copies large contiguous chunks of every
+// partial and adds them in registers, the concat moves tiles from the shards
+// to their place in the output without touching registers.
 #pragma once
 
 #include "tp_device.cuh"
 
 namespace tpk {
 
-__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) { return __ldcs(p); }
-
 __device__ __forceinline__ void add4(float4 &a, const float4 &b) {
     a.x += b.x;
     a.y += b.y;
     a.z += b.z;
     a.w += b.w;
-}
-
-// Each thread owns 8 consecutive output elements per step: it loads the 8
-// fp32 values of every shard (2 x 16 bytes per shard, all loads issued before
-// the first add when NS is a compile-time constant), adds them in ascending
-// shard order and stores 16 bytes (bf16) or 32 bytes (fp32).  Lanes never
-// need each other's data, so no cross-lane combine is required.
-template <int NS, bool OUT_BF16>
-__global__ void __launch_bounds__(256) shard_reduce_kernel(const float *__restrict__ P,
-                                                           void *__restrict__ Y, int64_t n_vec8,
-                                                           int64_t shard_stride, int n_shards) {
-    const int ns = NS > 0 ? NS : n_shards;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const float4 *P4 = reinterpret_cast<const float4 *>(P);
-    const int64_t s4 = shard_stride / 4;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < n_vec8;
-         v += step) {
-        float4 a0, a1;
-        if constexpr (NS > 0) {
-            float4 t[NS][2];
-#pragma unroll
-            for (int s = 0; s < NS; ++s) {
-                t[s][0] = ld_stream_f4(P4 + s * s4 + 2 * v);
-                t[s][1] = ld_stream_f4(P4 + s * s4 + 2 * v + 1);
-            }
-            a0 = t[0][0];
-            a1 = t[0][1];
-#pragma unroll
-            for (int s = 1; s < NS; ++s) {
-                add4(a0, t[s][0]);
-                add4(a1, t[s][1]);
-            }
-        } else {
-            a0 = ld_stream_f4(P4 + 2 * v);
-            a1 = ld_stream_f4(P4 + 2 * v + 1);
-            for (int s = 1; s < ns; ++s) {
-                add4(a0, ld_stream_f4(P4 + s * s4 + 2 * v));
-                add4(a1, ld_stream_f4(P4 + s * s4 + 2 * v + 1));
-            }
-        }
-        if constexpr (OUT_BF16) {
-            uint4 u = make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
-                                 pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
-            reinterpret_cast<uint4 *>(Y)[v] = u;
-        } else {
-            float4 *y4 = reinterpret_cast<float4 *>(Y);
-            y4[2 * v] = a0;
-            y4[2 * v + 1] = a1;
-        }
-    }
 }
 
 // Streaming reduce through shared memory: a persistent kernel, one CTA per
@@ -210,25 +158,98 @@ __global__ void shard_reduce_scalar_kernel(const float *__restrict__ P, void *__
     }
 }
 
-// Concat: grid.y walks output rows, grid.x x threads walk the 16-byte vectors
-// of a row.  Output vector cv of a row decomposes into (column group b,
-// shard i, offset j) with two multiply-high divisions; the source is vector
-// b*swv + j of row `row` of shard i.  Stores are row-contiguous, loads are
-// contiguous within each shard's run.
-__global__ void __launch_bounds__(256) shard_concat_kernel(const uint4 *__restrict__ Ys,
-                                                           uint4 *__restrict__ Y, int64_t rows,
-                                                           uint32_t ncv, FastDiv gwv, FastDiv swv,
-                                                           uint32_t nlv) {
-    const uint32_t cv = blockIdx.x * blockDim.x + threadIdx.x;
-    if (cv >= ncv) return;
-    const uint32_t b = fastdiv(cv, gwv);
-    const uint32_t rem = cv - b * gwv.d;
-    const uint32_t i = fastdiv(rem, swv);
-    const uint32_t j = rem - i * swv.d;
-    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
-        const uint4 v = __ldcs(Ys + (static_cast<int64_t>(i) * rows + row) * nlv + b * swv.d + j);
-        __stcs(Y + row * ncv + cv, v);
+// Concat through shared memory with tiled TMA copies: a persistent kernel,
+// one CTA (one working thread) per SM.  A unit is a box of `box_rows` rows x
+// `box_cols` columns of one column group b of one shard i: loaded from Ys
+// (viewed as [n][rows][shard_cols]) at (b*sw + j0, r0, i) and stored to Y
+// (viewed as [rows][n*shard_cols]) at (b*gw + i*sw + j0, r0); the bytes never
+// pass through registers.  Loads run CAT_LAG units ahead of stores in a
+// CAT_STAGES-deep ring; a stage is reused once the store that read it has
+// left shared memory.  Rows past the end are zero-filled by the load and
+// clipped by the store.
+constexpr int CAT_STAGES = 12;
+constexpr int CAT_LAG = 8;
+constexpr int CAT_BOX_BYTES = 16 * 1024;
+constexpr int CAT_SMEM_BYTES = CAT_STAGES * CAT_BOX_BYTES + 128;
+
+struct CatArgs {
+    int n, groups;         // shards, column groups
+    int sw, gw;            // columns a shard owns per group, output columns per group (n*sw)
+    int box_cols, box_rows;
+    int col_boxes;         // sw / box_cols
+    int64_t units;         // row blocks * n * groups * col_boxes
+    uint32_t box_bytes;
+    uint64_t wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(32, 1)
+    shard_concat_tma_kernel(const __grid_constant__ CUtensorMap tmSrc,
+                            const __grid_constant__ CUtensorMap tmDst, const CatArgs a) {
+    extern __shared__ __align__(128) uint8_t cat_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(cat_smem + CAT_STAGES * CAT_BOX_BYTES);
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < CAT_STAGES; ++st) mbar_init(smem_u32(&full[st]), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmSrc);
+        tma_prefetch_desc(&tmDst);
     }
+    __syncwarp();
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
+    if (threadIdx.x != 0) return;
+
+    // this CTA's units: blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int64_t mine = a.units > blockIdx.x ? (a.units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    bool ok = true;
+    int64_t issued = 0, stored = 0;  // units loaded / stored so far
+    for (int64_t step = 0; step < mine + CAT_LAG && ok; ++step) {
+        if (step < mine) {
+            const int st = static_cast<int>(step % CAT_STAGES);
+            // the store of unit step - CAT_STAGES (issued CAT_LAG steps after
+            // its load) has left this stage: at most CAT_STAGES - 1 - CAT_LAG
+            // younger stores may still be reading
+            bulk_wait_read_n<CAT_STAGES - 1 - CAT_LAG>();
+            const int64_t u = blockIdx.x + step * gridDim.x;
+            int64_t t = u;
+            const int jb = static_cast<int>(t % a.col_boxes); t /= a.col_boxes;
+            const int b = static_cast<int>(t % a.groups); t /= a.groups;
+            const int i = static_cast<int>(t % a.n); t /= a.n;
+            const int r0 = static_cast<int>(t) * a.box_rows;
+            const uint32_t fb = smem_u32(&full[st]);
+            mbar_arrive_expect_tx(fb, a.box_bytes);
+            tma_load_3d(smem_u32(cat_smem + st * CAT_BOX_BYTES), &tmSrc, fb,
+                        b * a.sw + jb * a.box_cols, r0, i);
+            issued = step + 1;
+        }
+        const int64_t j = step - CAT_LAG;
+        if (j >= 0 && j < mine) {
+            const int st = static_cast<int>(j % CAT_STAGES);
+            const uint32_t par = static_cast<uint32_t>((j / CAT_STAGES) & 1);
+            if (!mbar_wait_bounded(smem_u32(&full[st]), par, a.wait_limit_ns, &abort_flag,
+                                   SITE_MMA_FULL)) {
+                ok = false;
+                break;
+            }
+            const int64_t u = blockIdx.x + j * gridDim.x;
+            int64_t t = u;
+            const int jb = static_cast<int>(t % a.col_boxes); t /= a.col_boxes;
+            const int b = static_cast<int>(t % a.groups); t /= a.groups;
+            const int i = static_cast<int>(t % a.n); t /= a.n;
+            const int r0 = static_cast<int>(t) * a.box_rows;
+            tma_store_3d(&tmDst, smem_u32(cat_smem + st * CAT_BOX_BYTES),
+                         b * a.gw + i * a.sw + jb * a.box_cols, r0, 0);
+            bulk_commit_group();
+            stored = j + 1;
+        }
+    }
+    // after an abort, loads issued but not stored must land before the CTA
+    // exits (at most CAT_LAG of them, each in its own stage)
+    for (int64_t j = stored; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&full[j % CAT_STAGES]),
+                        static_cast<uint32_t>((j / CAT_STAGES) & 1), a.wait_limit_ns);
+    bulk_wait0();
 }
 
 }  // namespace tpk

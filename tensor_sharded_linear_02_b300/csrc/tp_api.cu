@@ -77,7 +77,10 @@ tp_status device_info(DeviceInfo **out) {
                                  RED_SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(shard_reduce_bulk_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 RED_SMEM_BYTES) != cudaSuccess)
+                                 RED_SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(shard_concat_tma_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CAT_SMEM_BYTES) != cudaSuccess)
             return TP_ERR_CUDA;
         d.max_pairs = active_clusters(reinterpret_cast<const void *>(gemm_persistent_kernel<256>),
                                       2, Ring<256>::SMEM_BYTES);
@@ -129,7 +132,8 @@ EncodeTiledFn encode_fn() {
 // 3-D tensor map (bf16 unless f32), 128-byte swizzle, zero fill out of bounds.
 bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2, bool f32 = false) {
+               uint32_t b2, bool f32 = false,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -138,7 +142,7 @@ bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint6
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
               const_cast<void *>(base), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -151,7 +155,7 @@ struct MapKey {
     const void *base;
     uint64_t dims[3], strides[2];
     uint32_t box[3];
-    uint32_t f32;
+    uint32_t f32, swizzle;
 };
 
 struct MapEntry {
@@ -167,7 +171,8 @@ uint64_t g_map_clock = 0;
 
 bool encode_3d_cached(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-                      uint32_t b2, bool f32 = false) {
+                      uint32_t b2, bool f32 = false,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     MapKey k;
     std::memset(&k, 0, sizeof(k));
     k.base = base;
@@ -175,6 +180,7 @@ bool encode_3d_cached(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
     k.strides[0] = stride1_bytes; k.strides[1] = stride2_bytes;
     k.box[0] = b0; k.box[1] = b1; k.box[2] = b2;
     k.f32 = f32 ? 1u : 0u;
+    k.swizzle = static_cast<uint32_t>(swizzle);
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
         for (MapEntry &e : g_maps) {
@@ -185,7 +191,7 @@ bool encode_3d_cached(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
             }
         }
     }
-    if (!encode_3d(m, base, d0, d1, d2, stride1_bytes, stride2_bytes, b0, b1, b2, f32))
+    if (!encode_3d(m, base, d0, d1, d2, stride1_bytes, stride2_bytes, b0, b1, b2, f32, swizzle))
         return false;
     std::lock_guard<std::mutex> lock(g_map_mutex);
     MapEntry *victim = &g_maps[0];
@@ -438,20 +444,7 @@ tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_
             return TP_ERR_CUDA;
         return launch_status();
     }
-    if (total % 8 != 0) {
-        shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n);
-        return launch_status();
-    }
-    const int64_t nv = total / 8;
-    const int grid = reduce_grid(nv, sm_count);
-    switch (n) {
-        case 1: shard_reduce_kernel<1, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-        case 2: shard_reduce_kernel<2, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-        case 4: shard_reduce_kernel<4, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-        case 8: shard_reduce_kernel<8, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-        case 16: shard_reduce_kernel<16, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-        default: shard_reduce_kernel<0, BF16><<<grid, 256, 0, s>>>(P, Y, nv, total, n); break;
-    }
+    shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n);
     return launch_status();
 }
 
@@ -664,14 +657,48 @@ tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t
     const int64_t ncv = shard_cols * n_shards / vec;  // output vectors per row
     if (ncv > kInt32Max || rows > kInt32Max) return TP_ERR_SHAPE;
     if (rows == 0 || ncv == 0) return TP_OK;
-    const uint32_t swv = static_cast<uint32_t>(sw / vec);
-    const uint32_t gwv = swv * static_cast<uint32_t>(n_shards);
-    const uint32_t nlv = swv * static_cast<uint32_t>(col_groups);
-    const unsigned gx = static_cast<unsigned>((ncv + 255) / 256);
-    const unsigned gy = static_cast<unsigned>(rows < 65535 ? rows : 65535);
-    shard_concat_kernel<<<dim3(gx, gy), 256, 0, s>>>(
-        static_cast<const uint4 *>(Ys), static_cast<uint4 *>(Y), rows,
-        static_cast<uint32_t>(ncv), make_fastdiv(gwv), make_fastdiv(swv), nlv);
+    // boxes: the widest of 256, 128, ... columns dividing sw, rows to fill
+    // 16 KiB (at most 256)
+    int box_cols = 256;
+    while (box_cols > vec && sw % box_cols != 0) box_cols /= 2;
+    int box_rows = static_cast<int>(CAT_BOX_BYTES / (box_cols * es));
+    if (box_rows > 256) box_rows = 256;
+    DeviceInfo *dev = nullptr;
+    if ((st = device_info(&dev)) != TP_OK) return st;
+    const bool f32 = (t == TP_F32);
+    const int64_t sc = shard_cols, N = sc * n_shards;
+    CUtensorMap tmSrc, tmDst;
+    if (!encode_3d_cached(&tmSrc, Ys, sc, rows, n_shards, sc * es, rows * sc * es,
+                          static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows), 1, f32,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_3d_cached(&tmDst, Y, N, rows, 1, N * es, rows * N * es,
+                          static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows), 1, f32,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+        return TP_ERR_CUDA;
+    CatArgs a{};
+    a.n = n_shards;
+    a.groups = col_groups;
+    a.sw = static_cast<int>(sw);
+    a.gw = static_cast<int>(sw * n_shards);
+    a.box_cols = box_cols;
+    a.box_rows = box_rows;
+    a.col_boxes = static_cast<int>(sw / box_cols);
+    a.units = (rows + box_rows - 1) / box_rows * n_shards * col_groups * a.col_boxes;
+    a.box_bytes = static_cast<uint32_t>(box_cols * box_rows * es);
+    a.wait_limit_ns = wait_limit_ns();
+    cudaLaunchConfig_t cfg{};
+    const int64_t grid = a.units < dev->sm_count ? a.units : dev->sm_count;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.dynamicSmemBytes = CAT_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, shard_concat_tma_kernel, tmSrc, tmDst, a) != cudaSuccess)
+        return TP_ERR_CUDA;
     return launch_status();
 }
 

@@ -206,6 +206,13 @@ __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most N of this thread's committed bulk stores still read
+// shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_n() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Wait until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -437,28 +444,6 @@ __device__ __forceinline__ float gelu_f32(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Division by a run-time invariant 32-bit divisor with one multiply-high
-// (Granlund & Montgomery, "Division by Invariant Integers using
-// Multiplication", PLDI 1994, round-up variant).  Valid for dividends below
-// 2^31 and divisors >= 1.
-struct FastDiv {
-    uint32_t d, m, s;
-};
-
-static inline FastDiv make_fastdiv(uint32_t d) {
-    FastDiv f;
-    f.d = d;
-    uint32_t l = 0;
-    while ((1ull << l) < d) ++l;
-    f.s = l;
-    f.m = static_cast<uint32_t>((((1ull << 32) * ((1ull << l) - d)) / d) + 1ull);
-    return f;
-}
-
-__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv &f) {
-    return (__umulhi(n, f.m) + n) >> f.s;
 }
 
 }  // namespace tpk
