@@ -93,6 +93,13 @@ def _load():
         lib.orc_row_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
         lib.orc_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                       ctypes.c_int]
+        lib.orc_gelu_grad.argtypes = [ctypes.c_double]
+        lib.orc_gelu_grad.restype = ctypes.c_double
+        lib.orc_column_linear_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                                   _i64]
+        lib.orc_row_linear_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
+        lib.orc_mlp_block_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
+                                               _i64, _i64]
         lib.orc_shard_reduce.argtypes = [_fp, _dp, _i64, _i64, _i64]
         lib.orc_shard_concat.argtypes = [_dp, _dp, _i64, _i64, _i64, _i64]
         _lib = lib
@@ -201,6 +208,58 @@ def mlp_block(X, W1, W2, n_shards: int, mirror_h_bf16: bool = False) -> np.ndarr
     _load().orc_mlp_block(_ptr(X), _ptr(W1), _ptr(W2), _ptr(Y), M, d, f, n_shards,
                           1 if mirror_h_bf16 else 0)
     return Y
+
+
+# ------------------------------------------------------------- backward ----
+
+def gelu_grad(x) -> np.ndarray:
+    """GeLU'(x) = Phi(x) + x*phi(x), elementwise."""
+    a = _f64(x)
+    f = _load().orc_gelu_grad
+    return np.vectorize(f, otypes=[np.float64])(a) if a.size else a.copy()
+
+
+def column_linear_backward(X, W, dY, n_shards: int):
+    """Backward of the column-parallel linear ([TP-topic] Megatron-LM,
+    "Identity Operators": the forward identity on X is a sum over shards in
+    the backward).  Returns (dX [M,K], dW [K,N]); dW's column block i is
+    shard i's gradient, dX = sum_i dY_i . W_i^T in ascending shard order."""
+    X, W, dY = _f64(X), _f64(W), _f64(dY)
+    M, K = X.shape
+    _, N = W.shape
+    assert dY.shape == (M, N) and N % n_shards == 0
+    dX = np.empty((M, K)); dW = np.empty((K, N))
+    _load().orc_column_linear_backward(_ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), M, K, N,
+                                       n_shards)
+    return dX, dW
+
+
+def row_linear_backward(X, W, dY, n_shards: int):
+    """Backward of the row-parallel linear (the forward sum is an identity in
+    the backward: every shard receives the full dY).  Returns (dX [M,K],
+    dW [K,N]); shard i owns columns i of dX and rows i of dW."""
+    X, W, dY = _f64(X), _f64(W), _f64(dY)
+    M, K = X.shape
+    _, N = W.shape
+    assert dY.shape == (M, N) and K % n_shards == 0
+    dX = np.empty((M, K)); dW = np.empty((K, N))
+    _load().orc_row_linear_backward(_ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), M, K, N,
+                                    n_shards)
+    return dX, dW
+
+
+def mlp_block_backward(X, W1, W2, dY, n_shards: int):
+    """Backward of the MLP block for L = sum(Y * dY): returns (dX, dW1, dW2),
+    each shard recomputing its pre-activation, dX summed over shards in
+    ascending order ([TP-topic] Megatron-LM, "Identity Operators")."""
+    X, W1, W2, dY = _f64(X), _f64(W1), _f64(W2), _f64(dY)
+    M, d = X.shape
+    _, f = W1.shape
+    assert W2.shape == (f, d) and dY.shape == (M, d) and f % n_shards == 0
+    dX = np.empty((M, d)); dW1 = np.empty((d, f)); dW2 = np.empty((f, d))
+    _load().orc_mlp_block_backward(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dY), _ptr(dX), _ptr(dW1),
+                                   _ptr(dW2), M, d, f, n_shards)
+    return dX, dW1, dW2
 
 
 def shard_reduce(P) -> np.ndarray:

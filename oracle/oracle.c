@@ -22,6 +22,7 @@
  *
  * All matrices are row-major.  Y = X W with X [M,K], W [K,N], Y [M,N].
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -247,6 +248,143 @@ void orc_mlp_block(const double *X, const double *W1, const double *W2, double *
     free(W1i);
     free(Hi);
     free(Pi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass.  The pages give no formulas, only the structure: the       */
+/* identity operator that feeds every shard the same input in the forward  */
+/* pass becomes an all-reduce (a sum over shards) in the backward pass, and */
+/* the forward all-reduce becomes an identity (every shard receives the     */
+/* full output gradient) ([TP-topic] Megatron-LM, "Identity Operators");    */
+/* each shard computes the gradients of its own 1/N of the weights          */
+/* ([TP-topic] "Memory Distribution", gradient memory).  The gradients      */
+/* themselves are the chain rule for L = sum(Y * dY) written out shard by   */
+/* shard with the transposes copied out as matrices.                        */
+/* ------------------------------------------------------------------------ */
+
+/* GeLU'(x) = Phi(x) + x * phi(x), phi the standard normal density. */
+double orc_gelu_grad(double x)
+{
+    return 0.5 * erfc(-x / sqrt(2.0)) + x * exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+}
+
+/* T[c][r] = A[r][c] for A [R, C]. */
+static void transpose(const double *A, double *T, int64_t R, int64_t C)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            T[c * R + r] = A[r * C + c];
+}
+
+static double *alloc_d(int64_t n)
+{
+    return (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+}
+
+/* Column-parallel linear Y_i = X . W_i (columns [i*N/n, (i+1)*N/n) of W).
+ * Shard i receives its output columns dY_i of dY and computes
+ *   dW_i = X^T . dY_i      (its own weight block: columns of dW)
+ *   dX_i = dY_i . W_i^T    (a partial of the input gradient)
+ * and dX = sum_i dX_i in ascending i (the backward all-reduce). */
+void orc_column_linear_backward(const double *X, const double *W, const double *dY,
+                                double *dX, double *dW, int64_t M, int64_t K, int64_t N,
+                                int64_t n_shards)
+{
+    const int64_t ns = N / n_shards;
+    double *Xt = alloc_d(K * M), *Wi = alloc_d(K * ns), *Wit = alloc_d(ns * K);
+    double *dYi = alloc_d(M * ns), *dWi = alloc_d(K * ns), *dXi = alloc_d(M * K);
+    transpose(X, Xt, M, K);
+    for (int64_t t = 0; t < M * K; ++t)
+        dX[t] = 0.0;
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t j = 0; j < ns; ++j)
+                Wi[k * ns + j] = W[k * N + i * ns + j];
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t j = 0; j < ns; ++j)
+                dYi[r * ns + j] = dY[r * N + i * ns + j];
+        orc_matmul(Xt, dYi, dWi, K, M, ns);
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t j = 0; j < ns; ++j)
+                dW[k * N + i * ns + j] = dWi[k * ns + j];
+        transpose(Wi, Wit, K, ns);
+        orc_matmul(dYi, Wit, dXi, M, ns, K);
+        for (int64_t t = 0; t < M * K; ++t)
+            dX[t] += dXi[t];
+    }
+    free(Xt); free(Wi); free(Wit); free(dYi); free(dWi); free(dXi);
+}
+
+/* Row-parallel linear Y = sum_i X_i . W_i (rows [i*K/n, (i+1)*K/n) of W and
+ * the same columns of X).  Every shard receives the full dY and computes
+ *   dW_i = X_i^T . dY      (its own weight block: rows of dW)
+ *   dX_i = dY . W_i^T      (its own columns of dX; no exchange). */
+void orc_row_linear_backward(const double *X, const double *W, const double *dY,
+                             double *dX, double *dW, int64_t M, int64_t K, int64_t N,
+                             int64_t n_shards)
+{
+    const int64_t ks = K / n_shards;
+    double *Xi = alloc_d(M * ks), *Xit = alloc_d(ks * M), *Wit = alloc_d(N * ks);
+    double *dWi = alloc_d(ks * N), *dXi = alloc_d(M * ks);
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t k = 0; k < ks; ++k)
+                Xi[r * ks + k] = X[r * K + i * ks + k];
+        transpose(Xi, Xit, M, ks);
+        orc_matmul(Xit, dY, dWi, ks, M, N);
+        memcpy(dW + i * ks * N, dWi, sizeof(double) * (size_t)(ks * N));
+        transpose(W + i * ks * N, Wit, ks, N);
+        orc_matmul(dY, Wit, dXi, M, N, ks);
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t k = 0; k < ks; ++k)
+                dX[r * K + i * ks + k] = dXi[r * ks + k];
+    }
+    free(Xi); free(Xit); free(Wit); free(dWi); free(dXi);
+}
+
+/* MLP block Y = sum_i GeLU(X . W1_i) . W2_i.  Shard i recomputes
+ * Z_i = X . W1_i and H_i = GeLU(Z_i), receives the full dY, and computes
+ *   dW2_i = H_i^T . dY                 (rows i of dW2)
+ *   dZ_i  = (dY . W2_i^T) * GeLU'(Z_i) (elementwise; no exchange)
+ *   dW1_i = X^T . dZ_i                 (columns i of dW1)
+ *   dX    = sum_i dZ_i . W1_i^T        (ascending i: the backward all-reduce) */
+void orc_mlp_block_backward(const double *X, const double *W1, const double *W2,
+                            const double *dY, double *dX, double *dW1, double *dW2,
+                            int64_t M, int64_t d, int64_t f, int64_t n_shards)
+{
+    const int64_t fs = f / n_shards;
+    double *Xt = alloc_d(d * M), *W1i = alloc_d(d * fs), *W1it = alloc_d(fs * d);
+    double *W2it = alloc_d(d * fs), *Zi = alloc_d(M * fs), *Hit = alloc_d(fs * M);
+    double *dHi = alloc_d(M * fs), *dWi = alloc_d((d > fs ? d : fs) * (d > fs ? fs : d));
+    double *dXi = alloc_d(M * d);
+    transpose(X, Xt, M, d);
+    for (int64_t t = 0; t < M * d; ++t)
+        dX[t] = 0.0;
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t k = 0; k < d; ++k)
+            for (int64_t j = 0; j < fs; ++j)
+                W1i[k * fs + j] = W1[k * f + i * fs + j];
+        orc_matmul(X, W1i, Zi, M, d, fs);
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t j = 0; j < fs; ++j)
+                Hit[j * M + r] = orc_gelu(Zi[r * fs + j]);
+        orc_matmul(Hit, dY, dWi, fs, M, d);                  /* dW2_i [fs, d] */
+        memcpy(dW2 + i * fs * d, dWi, sizeof(double) * (size_t)(fs * d));
+        transpose(W2 + i * fs * d, W2it, fs, d);
+        orc_matmul(dY, W2it, dHi, M, d, fs);                 /* dH_i [M, fs] */
+        for (int64_t t = 0; t < M * fs; ++t)
+            dHi[t] *= orc_gelu_grad(Zi[t]);                  /* dZ_i */
+        orc_matmul(Xt, dHi, dWi, d, M, fs);                  /* dW1_i [d, fs] */
+        for (int64_t k = 0; k < d; ++k)
+            for (int64_t j = 0; j < fs; ++j)
+                dW1[k * f + i * fs + j] = dWi[k * fs + j];
+        transpose(W1i, W1it, d, fs);
+        orc_matmul(dHi, W1it, dXi, M, fs, d);                /* dX_i [M, d] */
+        for (int64_t t = 0; t < M * d; ++t)
+            dX[t] += dXi[t];
+    }
+    free(Xt); free(W1i); free(W1it); free(W2it); free(Zi); free(Hit); free(dHi); free(dWi);
+    free(dXi);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -271,6 +271,110 @@ def test_concat_against_numpy():
     np.testing.assert_array_equal(oracle.shard_concat(Ys), np.concatenate(list(Ys), axis=1))
 
 
+# ------------------------------------------------------------- backward ----
+
+def test_gelu_grad_against_finite_differences():
+    """GeLU' against central differences of the oracle's own GeLU (truncation
+    error ~ h^2 times the third derivative, about 1e-10 here), its value at 0
+    and the identity GeLU'(z) + GeLU'(-z) = 1 (Phi(z) + Phi(-z) = 1 and
+    z*phi(z) is odd)."""
+    x = np.linspace(-8.0, 8.0, 321)
+    h = 1e-5
+    fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+    np.testing.assert_allclose(oracle.gelu_grad(x), fd, rtol=0, atol=1e-8)
+    assert oracle.gelu_grad([0.0])[0] == 0.5
+    np.testing.assert_allclose(oracle.gelu_grad(x) + oracle.gelu_grad(-x), 1.0, atol=1e-15)
+
+
+def _loss_column(X, W, dY, n):
+    Y, _ = oracle.column_linear(X, W, n)
+    return float(np.sum(Y * dY))
+
+
+def _loss_row(X, W, dY, n):
+    Y, _ = oracle.row_linear(X, W, n)
+    return float(np.sum(Y * dY))
+
+
+@pytest.mark.parametrize("kind", ["column", "row"])
+def test_linear_backward_is_the_forward_derivative(kind):
+    """L(X, W) = sum(Y * dY) is linear in X and in W separately, so on small
+    integers the change of the forward oracle's L along any integer direction
+    E equals <grad, E> exactly.  Checked for every shard count dividing the
+    split axis, plus: the sharded gradients equal the one-shard ones."""
+    rng = np.random.default_rng(11)
+    for M, K, N in [(3, 4, 6), (5, 6, 4), (2, 8, 8)]:
+        X = rng.integers(-4, 5, (M, K)).astype(float)
+        W = rng.integers(-4, 5, (K, N)).astype(float)
+        dY = rng.integers(-4, 5, (M, N)).astype(float)
+        axis = N if kind == "column" else K
+        back = oracle.column_linear_backward if kind == "column" else oracle.row_linear_backward
+        loss = _loss_column if kind == "column" else _loss_row
+        ref = back(X, W, dY, 1)
+        for n in [s for s in range(1, axis + 1) if axis % s == 0]:
+            dX, dW = back(X, W, dY, n)
+            np.testing.assert_array_equal(dX, ref[0])
+            np.testing.assert_array_equal(dW, ref[1])
+            for _ in range(3):
+                EX = rng.integers(-3, 4, X.shape).astype(float)
+                EW = rng.integers(-3, 4, W.shape).astype(float)
+                assert loss(X + EX, W, dY, n) - loss(X, W, dY, n) == float(np.sum(dX * EX))
+                assert loss(X, W + EW, dY, n) - loss(X, W, dY, n) == float(np.sum(dW * EW))
+
+
+def test_mlp_backward_against_finite_differences():
+    """dX, dW1, dW2 of the MLP block against central differences of the
+    forward oracle's L = sum(Y * dY) along random directions (relative error
+    of the difference quotient ~ h^2 ~ 1e-10), for 1, 2 and 4 shards; the
+    sharded gradients equal the one-shard ones up to reassociation."""
+    rng = np.random.default_rng(5)
+    M, d, f = 5, 6, 8
+    X = rng.standard_normal((M, d))
+    W1 = rng.standard_normal((d, f)) * 0.5
+    W2 = rng.standard_normal((f, d)) * 0.5
+    dY = rng.standard_normal((M, d))
+    ref = oracle.mlp_block_backward(X, W1, W2, dY, 1)
+    h = 1e-5
+
+    def L(X_, W1_, W2_, n):
+        return float(np.sum(oracle.mlp_block(X_, W1_, W2_, n) * dY))
+
+    for n in (1, 2, 4):
+        dX, dW1, dW2 = oracle.mlp_block_backward(X, W1, W2, dY, n)
+        for got, want in zip((dX, dW1, dW2), ref):
+            np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+        for _ in range(3):
+            E = [rng.standard_normal(a.shape) for a in (X, W1, W2)]
+            fd = [
+                (L(X + h * E[0], W1, W2, n) - L(X - h * E[0], W1, W2, n)) / (2 * h),
+                (L(X, W1 + h * E[1], W2, n) - L(X, W1 - h * E[1], W2, n)) / (2 * h),
+                (L(X, W1, W2 + h * E[2], n) - L(X, W1, W2 - h * E[2], n)) / (2 * h),
+            ]
+            for g, e, q in zip((dX, dW1, dW2), E, fd):
+                assert abs(float(np.sum(g * e)) - q) <= 1e-7 * max(1.0, abs(q))
+
+
+def test_backward_pins_catch_planted_mistakes():
+    """Gradients with a dropped GeLU' factor or a missing shard in the
+    backward sum fail the finite-difference pin that the oracle passes."""
+    rng = np.random.default_rng(6)
+    M, d, f = 4, 4, 6
+    X, dY = rng.standard_normal((M, d)), rng.standard_normal((M, d))
+    W1, W2 = rng.standard_normal((d, f)) * 0.5, rng.standard_normal((f, d)) * 0.5
+    h = 1e-5
+    EX = rng.standard_normal(X.shape)
+    fd = (np.sum(oracle.mlp_block(X + h * EX, W1, W2, 2) * dY)
+          - np.sum(oracle.mlp_block(X - h * EX, W1, W2, 2) * dY)) / (2 * h)
+    Z = oracle.matmul(X, W1)
+    gz = oracle.gelu_grad(Z)
+    no_grad_factor = oracle.matmul(oracle.matmul(dY, W2.T), W1.T)
+    one_shard_only = oracle.matmul(oracle.matmul(dY, W2[:3].T) * gz[:, :3], W1[:, :3].T)
+    dX, _, _ = oracle.mlp_block_backward(X, W1, W2, dY, 2)
+    assert abs(np.sum(dX * EX) - fd) < 1e-7 * max(1.0, abs(fd))
+    assert abs(np.sum(no_grad_factor * EX) - fd) > 1e-3
+    assert abs(np.sum(one_shard_only * EX) - fd) > 1e-3
+
+
 # ----------------------------------------------- inputs (generator) --------
 
 def test_generator_reproducible_and_shaped():
