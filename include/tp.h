@@ -251,6 +251,80 @@ tp_status tp_mlp_block_static_ws(const void *X, const void *W1, const void *W2, 
                                  int64_t M, int64_t d, int64_t f, int n_shards,
                                  tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
 
+/* ------------------------------------------------------------------------
+ * Backward pass.  The pages state the structure, not the formulas: the
+ * identity operator that feeds every shard the same input in the forward
+ * pass becomes an all-reduce -- here an on-device sum over shards -- in the
+ * backward pass, and the forward all-reduce becomes an identity: every
+ * shard receives the full output gradient (topic page, "Megatron-LM Tensor
+ * Parallelism", identity operators); each shard computes the gradients of
+ * its own 1/N of the weights (section "Memory Distribution").  For the loss
+ * gradient dY = dL/dY of Y = X W the gradients are dW = X^T dY and
+ * dX = dY W^T.
+ *
+ * Conventions as above; bf16 inputs only (TP_ERR_DTYPE otherwise), outputs
+ * bf16 (RNE) or fp32 (out_t), K and Nout multiples of 8.  Every gradient is
+ * a full dense matrix; a NULL output pointer skips that gradient.  All
+ * products run on the tensor cores with fp32 accumulation: X^T and W^T are
+ * read in place (the TMA boxes and shared-memory descriptors take the
+ * transposed layout), never copied.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Backward of tp_column_linear (act = none): X [M,K], W [K,Nout], dY [M,Nout].
+ *   dW [K, Nout] = X^T dY   -- column block i of dW is shard i's gradient
+ *                              X^T dY_i;
+ *   dX [M, K]    = sum_i dY_i W_i^T -- the backward all-reduce, added inside
+ *                              the fp32 accumulator in ascending shard order
+ *                              (the K loop of dY W^T walks W's columns in
+ *                              order).
+ * Errors: TP_ERR_DIVISIBILITY if n_shards does not divide Nout.
+ */
+tp_status tp_column_linear_backward(const void *X, const void *W, const void *dY, void *dX,
+                                    void *dW, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                    tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
+ * Backward of tp_row_linear: X [M,K], W [K,Nout], dY [M,Nout] (every shard
+ * receives the full dY).
+ *   dW [K, Nout] = X^T dY   -- row block i of dW is shard i's gradient X_i^T dY;
+ *   dX [M, K]    = dY W^T   -- column block i of dX is shard i's dY W_i^T
+ *                              (no exchange).
+ * The two products are the same as tp_column_linear_backward's; the split
+ * only decides which blocks a shard owns.
+ * Errors: TP_ERR_DIVISIBILITY if n_shards does not divide K.
+ */
+tp_status tp_row_linear_backward(const void *X, const void *W, const void *dY, void *dX,
+                                 void *dW, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                 tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
+ * Bytes of workspace tp_mlp_block_backward needs: three bf16 [M, f] buffers
+ * (pre-activation Z, H = GeLU(Z), dZ), each rounded up to 256 bytes.
+ * Returns 0 for negative sizes or t other than TP_BF16.
+ */
+size_t tp_mlp_block_backward_workspace_size(int64_t M, int64_t f, tp_dtype t);
+
+/*
+ * Backward of tp_mlp_block for dY [M, d], with the pre-activation recomputed
+ * (nothing saved from the forward pass):
+ *   Z   = X W1, H = GeLU(Z)        one launch, both stored bf16 (H equals
+ *                                  the forward pass's H bit for bit)
+ *   dZ  = (dY W2^T) * GeLU'(Z)     GeLU' = Phi + z phi fused into the
+ *                                  epilogue, Z read by TMA; stored bf16
+ *   dW2 = H^T dY   [f, d]          row block i = shard i
+ *   dW1 = X^T dZ   [d, f]          column block i = shard i
+ *   dX  = dZ W1^T  [M, d]          shards added in ascending order in the
+ *                                  fp32 accumulator (backward all-reduce)
+ * ws: at least tp_mlp_block_backward_workspace_size(M, f, in_t) bytes,
+ * 16-byte aligned, caller-owned; its contents are not needed afterwards.
+ * Any of dX, dW1, dW2 may be NULL.  Errors: as tp_mlp_block.
+ */
+tp_status tp_mlp_block_backward(const void *X, const void *W1, const void *W2, const void *dY,
+                                void *dX, void *dW1, void *dW2, void *ws, size_t ws_bytes,
+                                int64_t M, int64_t d, int64_t f, int n_shards, tp_dtype in_t,
+                                tp_dtype out_t, cudaStream_t s);
+
 /*
  * Synchronises stream s, then reads and clears the current device's status
  * word.  Returns TP_ERR_DEVICE_TIMEOUT if any kernel of this library gave up

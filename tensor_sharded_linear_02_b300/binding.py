@@ -54,6 +54,13 @@ SIGNATURES = {
                       _int, _vp], _int),
     "tp_mlp_block_static_ws": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
                                _int),
+    "tp_column_linear_backward": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int,
+                                   _vp], _int),
+    "tp_row_linear_backward": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
+                               _int),
+    "tp_mlp_block_backward_workspace_size": ([_i64, _i64, _int], ctypes.c_size_t),
+    "tp_mlp_block_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i64, _i64,
+                               _i64, _int, _int, _int, _vp], _int),
     "tp_get_device_status": ([_vp], _int),
     "tp_selftest_bounded_wait": ([ctypes.c_uint64, _vp], _int),
     "tp_status_string": ([_int], ctypes.c_char_p),
@@ -187,6 +194,46 @@ def tp_mlp_block(X, W1, W2, Y, ws, n_shards=1, stream=None):
                             ws.numel() * ws.element_size(), M, d, f, n_shards,
                             _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
     _check("tp_mlp_block", st)
+
+
+def _grad_dtype(*ts):
+    for t in ts:
+        if t is not None:
+            return _dtype_code(t.dtype)
+    return TP_F32
+
+
+def tp_column_linear_backward(X, W, dY, dX=None, dW=None, n_shards=1, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_column_linear_backward(_ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), M, K, N,
+                                         n_shards, _dtype_code(X.dtype), _grad_dtype(dX, dW),
+                                         _stream(stream))
+    _check("tp_column_linear_backward", st)
+
+
+def tp_row_linear_backward(X, W, dY, dX=None, dW=None, n_shards=1, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_row_linear_backward(_ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), M, K, N,
+                                      n_shards, _dtype_code(X.dtype), _grad_dtype(dX, dW),
+                                      _stream(stream))
+    _check("tp_row_linear_backward", st)
+
+
+def tp_mlp_block_backward_workspace_size(M, f, dtype) -> int:
+    return int(lib().tp_mlp_block_backward_workspace_size(M, f, _dtype_code(dtype)))
+
+
+def tp_mlp_block_backward(X, W1, W2, dY, ws, dX=None, dW1=None, dW2=None, n_shards=1,
+                          stream=None):
+    M, d = X.shape
+    f = W1.shape[1]
+    st = lib().tp_mlp_block_backward(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dY), _ptr(dX), _ptr(dW1),
+                                     _ptr(dW2), _ptr(ws), ws.numel() * ws.element_size(), M, d, f,
+                                     n_shards, _dtype_code(X.dtype), _grad_dtype(dX, dW1, dW2),
+                                     _stream(stream))
+    _check("tp_mlp_block_backward", st)
 
 
 def tp_mlp_block_static_ws(X, W1, W2, Y, n_shards=1, stream=None):

@@ -109,11 +109,18 @@ struct SmemBarriers {
     uint64_t empty[MAX_STAGES];  // both CTAs: stage consumed (multicast commit)
     uint64_t acc_full[2];        // both CTAs: accumulator ready (multicast commit)
     uint64_t acc_empty[2];       // even CTA: epilogue warps of both CTAs done
+    uint64_t aux_full[EPI_WARPS];  // per epilogue warp: an auxiliary input box landed
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
 };
 static_assert(sizeof(SmemBarriers) <= 256, "barrier block");
+
+// Epilogue modes of the TMA-store path (bf16 outputs):
+//   EPI_PLAIN      out = act(acc)                      -> tmC
+//   EPI_DUAL       out = acc -> tmC, and GeLU(acc)      -> tmAux
+//   EPI_GELU_GRAD  out = acc * GeLU'(z), z read from tmAux (same shape as out)
+enum EpiMode : int { EPI_PLAIN = 0, EPI_DUAL = 1, EPI_GELU_GRAD = 2 };
 
 // Bytes both CTAs of a pair land per k-block of a bn-wide tile.
 __host__ __device__ constexpr uint32_t pair_stage_tx(int bn) {
@@ -134,6 +141,7 @@ struct GemmArgs {
     int act_gelu;
     int tma_store;       // 1: the plain output goes through shared memory and TMA
                          //    stores (tensor map tmC); 0: per-thread vector stores
+    int epi;             // EPI_PLAIN, EPI_DUAL or EPI_GELU_GRAD (TMA-store path, bf16)
     void *out_shards;    // optional shard-major copy (column split)
     int shard_sw;        // columns a shard owns in each column group
     int shard_gw;        // columns per column group
@@ -300,6 +308,89 @@ __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool 
     }
 }
 
+// Dual epilogue (bf16): the raw accumulator to tmC and its GeLU to tmAux,
+// 64 columns at a time.
+__device__ __forceinline__ void epilogue_dual(const CUtensorMap *tmC, const CUtensorMap *tmAux,
+                                              uint32_t taddr, uint32_t stg, int row0, int col_base,
+                                              int cofs, int ncols, uint32_t acc_empty_addr) {
+#pragma unroll 1
+    for (int c = 0; c < ncols; c += 64) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(taddr + cofs + c, r0);
+        tmem_ld_32x32b_x32(taddr + cofs + c + 32, r1);
+        tmem_ld_wait();
+        if (c + 64 >= ncols) release_accumulator(acc_empty_addr);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            pk[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+        }
+        stage_and_store_box(tmC, stg, pk, col_base + cofs + c, row0, 0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2(gelu_f32(__uint_as_float(r0[2 * i])),
+                                gelu_f32(__uint_as_float(r0[2 * i + 1])));
+            pk[16 + i] = pack_bf16x2(gelu_f32(__uint_as_float(r1[2 * i])),
+                                     gelu_f32(__uint_as_float(r1[2 * i + 1])));
+        }
+        stage_and_store_box(tmAux, stg, pk, col_base + cofs + c, row0, 0);
+    }
+}
+
+// GeLU-gradient epilogue (bf16): out = acc * GeLU'(z).  For each 64-column
+// box, lane 0 loads the matching box of z (bf16, same swizzled 32 x 128-byte
+// layout as the store box) into the warp's store buffer with TMA, counted on
+// the warp's aux barrier; each lane then reads its own row of z, multiplies,
+// and writes the result over it, and the box leaves with one TMA store.
+// `aux_count` counts the boxes this warp has loaded (the barrier's phase).
+__device__ __forceinline__ bool epilogue_gelu_grad(const CUtensorMap *tmC,
+                                                   const CUtensorMap *tmAux, SmemBarriers *bars,
+                                                   int ew, uint32_t &aux_count, uint32_t taddr,
+                                                   uint32_t stg, int row0, int col_base, int cofs,
+                                                   int ncols, uint32_t acc_empty_addr,
+                                                   uint64_t limit) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t bar = smem_u32(&bars->aux_full[ew]);
+#pragma unroll 1
+    for (int c = 0; c < ncols; c += 64) {
+        const int col = col_base + cofs + c;
+        if (lane == 0) {
+            bulk_wait_read0();  // the previous box has left the buffer
+            mbar_arrive_expect_tx(bar, STG_BYTES);
+            tma_load_3d(stg, tmAux, bar, col, row0, 0);
+        }
+        __syncwarp();
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(taddr + cofs + c, r0);
+        tmem_ld_32x32b_x32(taddr + cofs + c + 32, r1);
+        tmem_ld_wait();
+        if (c + 64 >= ncols) release_accumulator(acc_empty_addr);
+        const bool ok = mbar_wait_warp(bar, aux_count & 1u, limit, &bars->abort,
+                                       SITE_EPI_ACC_FULL);
+        ++aux_count;
+        if (!ok) return false;
+        uint32_t pk[32];
+        const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // 16-byte chunk q = columns 8q .. 8q+7
+            const uint4 zv = ld_shared_v4(row_addr + ((q ^ (lane & 7)) << 4));
+            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int i = 8 * q + 2 * h;  // column within the box
+                const float z0 = __uint_as_float(zw[h] << 16);
+                const float z1 = __uint_as_float(zw[h] & 0xffff0000u);
+                const float a0 = __uint_as_float(i < 32 ? r0[i] : r1[i - 32]);
+                const float a1 = __uint_as_float(i + 1 < 32 ? r0[i + 1] : r1[i - 31]);
+                pk[i / 2] = pack_bf16x2(a0 * gelu_grad_f32(z0), a1 * gelu_grad_f32(z1));
+            }
+        }
+        stage_and_store_box(tmC, stg, pk, col, row0, 0);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_tile, int &n_tile,
                                             int &g) {
     const int tiles = a.m_tiles * a.n_tiles;
@@ -322,7 +413,11 @@ struct ProducerState {
     uint32_t issued = 0;  // 1 once any load was issued
 };
 
-template <int MAXBN>
+// A_MN: A is stored [K][M] (M contiguous; e.g. X^T of a weight gradient),
+// loaded as two 64-row x 128-k boxes.  B_KM: B is stored [N][K] (K
+// contiguous; e.g. W^T of an input gradient), loaded as two 64-k x bn/2-row
+// boxes.  Otherwise A is [M][K] and B is [K][N].
+template <int MAXBN, bool A_MN = false, bool B_KM = false>
 __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                                 uint8_t *ring, SmemBarriers *bars,
                                                 uint32_t full_remote, bool leader, int half,
@@ -342,12 +437,24 @@ __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CU
         uint8_t *sa = ring + ps.stage * R::STAGE_BYTES;
         uint8_t *sb = sa + A_STAGE_BYTES;
 #pragma unroll
-        for (int j = 0; j < BK / BK_BOX; ++j)
-            tma_load_3d_pair(smem_u32(sa + j * A_BOX_BYTES), tmA, fb, kb * BK + j * BK_BOX, g,
-                             row0);
-        for (int j = 0; j < chunks; ++j)
-            tma_load_3d_pair(smem_u32(sb + j * B_CHUNK_BYTES), tmB, fb, col0 + j * B_CHUNK_N,
-                             kb * BK, g);
+        for (int j = 0; j < BK / BK_BOX; ++j) {
+            if (A_MN)
+                tma_load_3d_pair(smem_u32(sa + j * A_BOX_BYTES), tmA, fb, row0 + j * 64, kb * BK,
+                                 0);
+            else
+                tma_load_3d_pair(smem_u32(sa + j * A_BOX_BYTES), tmA, fb, kb * BK + j * BK_BOX, g,
+                                 row0);
+        }
+        if (B_KM) {
+#pragma unroll
+            for (int j = 0; j < BK / BK_BOX; ++j)
+                tma_load_3d_pair(smem_u32(sb + j * (bn / 2) * BK_BOX * 2), tmB, fb,
+                                 kb * BK + j * BK_BOX, col0, 0);
+        } else {
+            for (int j = 0; j < chunks; ++j)
+                tma_load_3d_pair(smem_u32(sb + j * B_CHUNK_BYTES), tmB, fb, col0 + j * B_CHUNK_N,
+                                 kb * BK, g);
+        }
         ps.issued = 1;
         if (++ps.stage == R::STAGES) {
             ps.stage = 0;
@@ -396,26 +503,34 @@ __device__ __forceinline__ void producer_drain(const ProducerState &ps) {
 // The operands arrive through the async proxy (TMA) and are read through it
 // (tcgen05.mma), so the full-barrier wait alone orders them; no tcgen05
 // fence is needed per k-block.
-template <int MAXBN>
+// With A_MN the A stage is two 64-row chunks (LBO 16 KiB) of 128 k-rows and
+// a K step adds two 8-row groups (128); with B_KM the B stage is two 64-k
+// boxes of bn/2 rows, like A's K-major layout.
+template <int MAXBN, bool A_MN = false, bool B_KM = false>
 __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, int &stage,
                                             uint32_t &phase, uint32_t d_tmem, uint32_t idesc,
-                                            uint16_t pair_mask, int kb0, int kb1,
+                                            uint16_t pair_mask, int kb0, int kb1, int bn,
                                             uint64_t limit) {
     using R = Ring<MAXBN>;
-    const uint64_t a_ring = smem_desc_sw128(smem_u32(ring), 16, A_SBO);
-    const uint64_t b_ring = smem_desc_sw128(smem_u32(ring) + A_STAGE_BYTES, B_LBO, B_SBO);
+    const uint64_t a_ring = A_MN ? smem_desc_sw128(smem_u32(ring), A_BOX_BYTES, A_SBO)
+                                 : smem_desc_sw128(smem_u32(ring), 16, A_SBO);
+    const uint64_t b_ring = B_KM ? smem_desc_sw128(smem_u32(ring) + A_STAGE_BYTES, 16, B_SBO)
+                                 : smem_desc_sw128(smem_u32(ring) + A_STAGE_BYTES, B_LBO, B_SBO);
+    const uint64_t b_box = static_cast<uint64_t>(((bn / 2) * BK_BOX * 2) >> 4);
     for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&bars->full[stage]), phase, limit, &bars->abort,
                                SITE_MMA_FULL))
             return false;
         const uint64_t so = static_cast<uint64_t>(stage * (R::STAGE_BYTES >> 4));
         const uint64_t da = a_ring + so, db = b_ring + so;
-        constexpr int KPB = BK_BOX / UMMA_K;  // K steps per A box
-        umma_f16_pair(d_tmem, da, db, idesc, kb > kb0 ? 1u : 0u);
+        constexpr int KPB = BK_BOX / UMMA_K;  // K steps per 64-deep box
 #pragma unroll
-        for (int k = 1; k < BK / UMMA_K; ++k)
-            umma_f16_pair(d_tmem, da + (A_BOX_BYTES >> 4) * (k / KPB) + 2 * (k % KPB),
-                          db + 128 * k, idesc, 1u);
+        for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ak = A_MN ? da + 128 * k
+                                     : da + (A_BOX_BYTES >> 4) * (k / KPB) + 2 * (k % KPB);
+            const uint64_t bk = B_KM ? db + b_box * (k / KPB) + 2 * (k % KPB) : db + 128 * k;
+            umma_f16_pair(d_tmem, ak, bk, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
         umma_commit_pair_mc(smem_u32(&bars->empty[stage]), pair_mask);
         if (++stage == R::STAGES) {
             stage = 0;
@@ -451,6 +566,7 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, int stages, uint3
             mbar_init(smem_u32(&bars->acc_full[i]), 1);
             mbar_init(smem_u32(&bars->acc_empty[i]), 2 * EPI_WARPS);
         }
+        for (int i = 0; i < EPI_WARPS; ++i) mbar_init(smem_u32(&bars->aux_full[i]), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -485,11 +601,12 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, uint32_t tmem_
 // ---------------------------------------------------------------------------
 // Persistent kernel: cluster = one pair, grid = 2 x (pairs launched).
 // ---------------------------------------------------------------------------
-template <int MAXBN>
+template <int MAXBN, bool A_MN = false, bool B_KM = false>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
+                           const __grid_constant__ CUtensorMap tmC,
+                           const __grid_constant__ CUtensorMap tmAux, const GemmArgs a) {
     using R = Ring<MAXBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = align1024(smem_raw);
@@ -504,8 +621,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int num_pairs = gridDim.x >> 1;
     const int bn = a.bn;
 
-    const CUtensorMap *maps[3] = {&tmA, &tmB, &tmC};
-    gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps, a.tma_store ? 3 : 2);
+    const CUtensorMap *maps[4] = {&tmA, &tmB, &tmC, &tmAux};
+    gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps,
+               a.epi != EPI_PLAIN ? 4 : (a.tma_store ? 3 : 2));
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
@@ -517,8 +635,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int u = pair; u < a.num_units && ok; u += num_pairs) {
                 int mt, nt, g;
                 decode_unit(a, u, mt, nt, g);
-                ok = produce_kblocks<MAXBN>(&tmA, &tmB, ring, bars, full_remote, leader, half, ps,
-                                            mt, nt, bn, g, 0, a.k_blocks, limit);
+                ok = produce_kblocks<MAXBN, A_MN, B_KM>(&tmA, &tmB, ring, bars, full_remote,
+                                                        leader, half, ps, mt, nt, bn, g, 0,
+                                                        a.k_blocks, limit);
             }
             if (ok) ok = producer_tail<MAXBN>(bars, ps, limit);
             if (!ok) producer_drain(ps);
@@ -526,7 +645,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (leader && lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(PAIR_M, bn, true);
+            const uint32_t idesc = idesc_bf16_f32(PAIR_M, bn, !B_KM, A_MN);
             int stage = 0, local = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -537,8 +656,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                        &bars->abort, SITE_MMA_ACC_EMPTY);
                 if (!ok) break;
                 tc_fence_after();
-                ok = mma_kblocks<MAXBN>(ring, bars, stage, phase, tmem_base + acc * ACC_STRIDE,
-                                        idesc, 0x3, 0, a.k_blocks, limit);
+                ok = mma_kblocks<MAXBN, A_MN, B_KM>(ring, bars, stage, phase,
+                                                    tmem_base + acc * ACC_STRIDE, idesc, 0x3, 0,
+                                                    a.k_blocks, bn, limit);
                 if (!ok) break;
                 umma_commit_pair_mc(smem_u32(&bars->acc_full[acc]), 0x3);
             }
@@ -550,6 +670,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int cofs = ((warp - 2) >> 2) * (bn / 2);  // this warp's half of the columns
         const uint32_t acc_empty_remote = dsmem_map(smem_u32(&bars->acc_empty[0]), 0);
         const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
+        uint32_t aux_count = 0;
         int local = 0;
         for (int u = pair; u < a.num_units; u += num_pairs, ++local) {
             const int acc = local & 1;
@@ -564,11 +685,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tmem_base + acc * ACC_STRIDE + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t release = acc_empty_remote + acc * 8;
             const int row0 = mt * PAIR_M + half * BM + q * 32;
-            if (a.tma_store)
+            if (a.epi == EPI_GELU_GRAD) {
+                if (!epilogue_gelu_grad(&tmC, &tmAux, bars, warp - 2, aux_count, taddr, stg, row0,
+                                        nt * bn, cofs, bn / 2, release, limit))
+                    break;
+            } else if (a.epi == EPI_DUAL) {
+                epilogue_dual(&tmC, &tmAux, taddr, stg, row0, nt * bn, cofs, bn / 2, release);
+            } else if (a.tma_store) {
                 epilogue_tma_store(&tmC, a.out_f32 != 0, a.act_gelu != 0, taddr, stg, row0,
                                    nt * bn, cofs, bn / 2, g, release);
-            else
+            } else {
                 epilogue_direct(a, taddr, row0 + lane, nt * bn, cofs, bn / 2, g, release);
+            }
         }
         if (lane == 0) bulk_wait0();  // every store box has left shared memory and landed
         __syncwarp();
@@ -629,7 +757,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             if (mma_kblocks<256>(ring, bars, stage, phase, tmem_base,
-                                 idesc_bf16_f32(PAIR_M, BN, true), pair_mask, kb0, kb1, limit))
+                                 idesc_bf16_f32(PAIR_M, BN, true), pair_mask, kb0, kb1, BN,
+                                 limit))
                 umma_commit_pair_mc(smem_u32(&bars->acc_full[0]), pair_mask);
             else
                 mma_drain(bars, limit);

@@ -69,6 +69,12 @@ tp_status device_info(DeviceInfo **out) {
             cudaFuncSetAttribute(gemm_persistent_kernel<128>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<128>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<256, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<256, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(gemm_cluster_sum_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<256>::SMEM_BYTES) != cudaSuccess ||
@@ -227,8 +233,8 @@ tp_status launch_status() {
 // -------------------------------------------------------------- launchers --
 
 struct GemmCall {
-    const void *A;  // [M, K] bf16 row-major
-    const void *B;  // [K, N] bf16 row-major
+    const void *A;  // [M, K] bf16 row-major, or [K, M] when a_mn
+    const void *B;  // [K, N] bf16 row-major, or [N, K] when b_km
     int64_t M, N, K;
     int k_groups;   // 1: one accumulator over all of K; n: one output per shard
     void *out;
@@ -238,6 +244,10 @@ struct GemmCall {
     void *out_shards;
     int n_shards, col_groups;
     bool allow_split;
+    bool a_mn = false;         // A stored transposed (M contiguous)
+    bool b_km = false;         // B stored transposed (K contiguous)
+    int epi = EPI_PLAIN;       // EPI_DUAL / EPI_GELU_GRAD use aux (bf16 [M, N])
+    void *aux = nullptr;
 };
 
 // Launch plan of one GEMM: tile width and, for the cluster split kernel,
@@ -311,13 +321,33 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     if (st != TP_OK) return st;
 
     const int64_t Kg = c.K / c.k_groups;
-    CUtensorMap tmA, tmB;
-    // A viewed as [M][k_groups][Kg]; box = 128 rows x 64 k of one group.
-    if (!encode_3d_cached(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK_BOX, 1, BM))
-        return TP_ERR_CUDA;
-    // B viewed as [k_groups][Kg][N]; box = 128 k-rows x 64 columns of one group.
-    if (!encode_3d_cached(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N, BK, 1))
-        return TP_ERR_CUDA;
+    const bool plain = !c.a_mn && !c.b_km && c.epi == EPI_PLAIN;
+    CUtensorMap tmA, tmB, tmAux;
+    if (c.a_mn) {
+        // A^T stored [K][M]: viewed as [1][K][M]; box = 128 k-rows x 64 columns.
+        if (!encode_3d_cached(&tmA, c.A, c.M, c.K, 1, c.M * 2, c.K * c.M * 2, 64, BK, 1))
+            return TP_ERR_CUDA;
+    } else {
+        // A viewed as [M][k_groups][Kg]; box = 128 rows x 64 k of one group.
+        if (!encode_3d_cached(&tmA, c.A, Kg, c.k_groups, c.M, Kg * 2, c.K * 2, BK_BOX, 1, BM))
+            return TP_ERR_CUDA;
+    }
+    if (c.b_km) {
+        // B^T stored [N][K]: viewed as [1][N][K]; box = 128 rows x 64 k.
+        if (!encode_3d_cached(&tmB, c.B, c.K, c.N, 1, c.K * 2, c.N * c.K * 2, BK_BOX, 128, 1))
+            return TP_ERR_CUDA;
+    } else {
+        // B viewed as [k_groups][Kg][N]; box = 128 k-rows x 64 columns of one group.
+        if (!encode_3d_cached(&tmB, c.B, c.N, Kg, c.k_groups, c.N * 2, Kg * c.N * 2, B_CHUNK_N,
+                              BK, 1))
+            return TP_ERR_CUDA;
+    }
+    std::memset(&tmAux, 0, sizeof(tmAux));
+    if (c.epi != EPI_PLAIN) {
+        // auxiliary bf16 [M, N], same boxes as the bf16 output
+        if (!encode_3d_cached(&tmAux, c.aux, c.N, c.M, 1, c.N * 2, c.M * c.N * 2, 64, 32, 1))
+            return TP_ERR_CUDA;
+    }
 
     // Output viewed as [k_groups][M][N]; box = 32 rows x 128 bytes of one group.
     CUtensorMap tmC;
@@ -333,11 +363,15 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
 
     GemmArgs a{};
     a.tma_store = tma_store ? 1 : 0;
+    a.epi = c.epi;
     a.M = static_cast<int>(c.M);
     a.N = static_cast<int>(c.N);
     a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
     a.k_groups = c.k_groups;
-    const GemmPlan plan = plan_gemm(c.M, c.N, a.k_blocks, c.k_groups, c.allow_split, c.gelu, *dev);
+    // transposed operands and the extra epilogues: persistent, 256 wide
+    const GemmPlan plan = plain ? plan_gemm(c.M, c.N, a.k_blocks, c.k_groups, c.allow_split,
+                                            c.gelu, *dev)
+                                : GemmPlan{256, 1};
     a.bn = plan.bn;
     a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
     a.n_tiles = static_cast<int>((c.N + a.bn - 1) / a.bn);
@@ -380,10 +414,16 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     cudaError_t e;
     if (S > 1)
         e = cudaLaunchKernelEx(&cfg, gemm_cluster_sum_kernel, tmA, tmB, tmC, a);
+    else if (c.a_mn)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, true, false>, tmA, tmB, tmC,
+                               tmAux, a);
+    else if (c.b_km)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, true>, tmA, tmB, tmC,
+                               tmAux, a);
     else if (a.bn == 128)
-        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<128>, tmA, tmB, tmC, a);
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<128>, tmA, tmB, tmC, tmAux, a);
     else
-        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256>, tmA, tmB, tmC, a);
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256>, tmA, tmB, tmC, tmAux, a);
     if (e != cudaSuccess) return TP_ERR_CUDA;
     return launch_status();
 }
@@ -769,6 +809,176 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, v
     a2.M = M; a2.K = f; a2.N = d; a2.k_shards = n_shards; a2.act_gelu = 0; a2.partials = nullptr;
     a2.shard_gw = d; a2.shard_sw = d; a2.shard_nl = d;
     return launch_simt(ws, W2, Y, nullptr, a2, TP_F32, out_t, s);
+}
+
+// ----------------------------------------------------------- backward ----
+
+namespace {
+
+// dW = X^T . dY  [K, N]  and  dX = dY . W^T  [M, K], bf16 inputs.  The two
+// products are the same for the column and the row split; only what a shard
+// owns differs (see include/tp.h).  Either output may be NULL.
+tp_status linear_backward_impl(const void *X, const void *W, const void *dY, void *dX, void *dW,
+                               int64_t M, int64_t K, int64_t N, tp_dtype in_t, tp_dtype out_t,
+                               cudaStream_t s) {
+    const size_t ot = dtype_size(out_t);
+    const size_t xb = M * K * 2, wb = K * N * 2, yb = M * N * 2;
+    const size_t dxb = M * K * ot, dwb = K * N * ot;
+    if (!present(X, xb) || !present(W, wb) || !present(dY, yb)) return TP_ERR_NULL;
+    if (in_t != TP_BF16 || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dY, 16) || !aligned(dX, 16) ||
+        !aligned(dW, 16) || K % 8 != 0 || N % 8 != 0)
+        return TP_ERR_ALIGNMENT;
+    const void *ins[3] = {X, W, dY};
+    const size_t inb[3] = {xb, wb, yb};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(dX, dxb, ins[i], inb[i]) || overlaps(dW, dwb, ins[i], inb[i]))
+            return TP_ERR_ALIAS;
+    if (overlaps(dX, dxb, dW, dwb)) return TP_ERR_ALIAS;
+    tp_status st;
+    if (dW && K > 0 && N > 0) {
+        if (M == 0) {
+            if (cudaMemsetAsync(dW, 0, dwb, s) != cudaSuccess) return TP_ERR_CUDA;
+        } else {
+            GemmCall c{};
+            c.A = X; c.a_mn = true;  // X^T: X is [M][K] = [K'][M'] with M' = K
+            c.B = dY;                // [M][N] = [K'][N']
+            c.M = K; c.N = N; c.K = M;
+            c.k_groups = 1; c.out = dW; c.out_f32 = (out_t == TP_F32);
+            c.n_shards = 1; c.col_groups = 1;
+            if ((st = launch_gemm(c, s)) != TP_OK) return st;
+        }
+    }
+    if (dX && M > 0 && K > 0) {
+        if (N == 0) {
+            if (cudaMemsetAsync(dX, 0, dxb, s) != cudaSuccess) return TP_ERR_CUDA;
+        } else {
+            GemmCall c{};
+            c.A = dY;                // [M][N]: K' = N walks the output columns (shards) in order
+            c.B = W; c.b_km = true;  // W^T: W is [K][N] = [N'][K'] with N' = K
+            c.M = M; c.N = K; c.K = N;
+            c.k_groups = 1; c.out = dX; c.out_f32 = (out_t == TP_F32);
+            c.n_shards = 1; c.col_groups = 1;
+            if ((st = launch_gemm(c, s)) != TP_OK) return st;
+        }
+    }
+    return TP_OK;
+}
+
+}  // namespace
+
+tp_status tp_column_linear_backward(const void *X, const void *W, const void *dY, void *dX,
+                                    void *dW, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                    tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    tp_status st = check_sizes(M, K, Nout);
+    if (st != TP_OK) return st;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    if (Nout % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    return linear_backward_impl(X, W, dY, dX, dW, M, K, Nout, in_t, out_t, s);
+}
+
+tp_status tp_row_linear_backward(const void *X, const void *W, const void *dY, void *dX,
+                                 void *dW, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                 tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    tp_status st = check_sizes(M, K, Nout);
+    if (st != TP_OK) return st;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    if (K % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    return linear_backward_impl(X, W, dY, dX, dW, M, K, Nout, in_t, out_t, s);
+}
+
+size_t tp_mlp_block_backward_workspace_size(int64_t M, int64_t f, tp_dtype t) {
+    if (M < 0 || f < 0 || t != TP_BF16) return 0;
+    return 3 * ((static_cast<size_t>(M) * static_cast<size_t>(f) * 2 + 255) &
+                ~static_cast<size_t>(255));
+}
+
+tp_status tp_mlp_block_backward(const void *X, const void *W1, const void *W2, const void *dY,
+                                void *dX, void *dW1, void *dW2, void *ws, size_t ws_bytes,
+                                int64_t M, int64_t d, int64_t f, int n_shards, tp_dtype in_t,
+                                tp_dtype out_t, cudaStream_t s) {
+    tp_status st = check_sizes(M, d, f);
+    if (st != TP_OK) return st;
+    if (in_t != TP_BF16 || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    if (f % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    const size_t ot = dtype_size(out_t);
+    const size_t xb = M * d * 2, w1b = d * f * 2, w2b = f * d * 2, yb = M * d * 2;
+    const size_t dxb = M * d * ot, dw1b = d * f * ot, dw2b = f * d * ot;
+    if (!present(X, xb) || !present(W1, w1b) || !present(W2, w2b) || !present(dY, yb))
+        return TP_ERR_NULL;
+    const size_t part = (static_cast<size_t>(M) * f * 2 + 255) & ~static_cast<size_t>(255);
+    const size_t need = tp_mlp_block_backward_workspace_size(M, f, in_t);
+    if (need > 0 && (!ws || ws_bytes < need)) return TP_ERR_WORKSPACE;
+    if (!aligned(X, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(dY, 16) ||
+        !aligned(dX, 16) || !aligned(dW1, 16) || !aligned(dW2, 16) || !aligned(ws, 16) ||
+        d % 8 != 0 || f % 8 != 0)
+        return TP_ERR_ALIGNMENT;
+    const void *ins[5] = {X, W1, W2, dY, ws};
+    const size_t inb[5] = {xb, w1b, w2b, yb, need};
+    void *outs[3] = {dX, dW1, dW2};
+    const size_t outb[3] = {dxb, dw1b, dw2b};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i])) return TP_ERR_ALIAS;
+        for (int p = o + 1; p < 3; ++p)
+            if (overlaps(outs[o], outb[o], outs[p], outb[p])) return TP_ERR_ALIAS;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(ws, need, ins[i], inb[i])) return TP_ERR_ALIAS;
+    if (M == 0 || d == 0 || f == 0) {
+        // empty contractions give zero gradients
+        if (dW1 && d > 0 && f > 0 && cudaMemsetAsync(dW1, 0, dw1b, s) != cudaSuccess)
+            return TP_ERR_CUDA;
+        if (dW2 && d > 0 && f > 0 && cudaMemsetAsync(dW2, 0, dw2b, s) != cudaSuccess)
+            return TP_ERR_CUDA;
+        if (dX && M > 0 && d > 0 && cudaMemsetAsync(dX, 0, dxb, s) != cudaSuccess)
+            return TP_ERR_CUDA;
+        return TP_OK;
+    }
+    uint8_t *Z = static_cast<uint8_t *>(ws), *H = Z + part, *dZ = H + part;
+    const bool f32 = (out_t == TP_F32);
+    // 1. recompute Z = X . W1 and H = GeLU(Z) (bf16, one launch)
+    {
+        GemmCall c{};
+        c.A = X; c.B = W1; c.M = M; c.N = f; c.K = d;
+        c.k_groups = 1; c.out = Z; c.epi = EPI_DUAL; c.aux = H;
+        c.n_shards = 1; c.col_groups = 1;
+        if ((st = launch_gemm(c, s)) != TP_OK) return st;
+    }
+    // 2. dZ = (dY . W2^T) * GeLU'(Z): every shard's block of columns of dZ
+    if (dW1 || dX) {
+        GemmCall c{};
+        c.A = dY; c.B = W2; c.b_km = true;  // W2 is [f][d] = [N'][K']
+        c.M = M; c.N = f; c.K = d;
+        c.k_groups = 1; c.out = dZ; c.epi = EPI_GELU_GRAD; c.aux = Z;
+        c.n_shards = 1; c.col_groups = 1;
+        if ((st = launch_gemm(c, s)) != TP_OK) return st;
+    }
+    // 3. dW2 = H^T . dY (rows block i = shard i)
+    if (dW2) {
+        GemmCall c{};
+        c.A = H; c.a_mn = true; c.B = dY; c.M = f; c.N = d; c.K = M;
+        c.k_groups = 1; c.out = dW2; c.out_f32 = f32; c.n_shards = 1; c.col_groups = 1;
+        if ((st = launch_gemm(c, s)) != TP_OK) return st;
+    }
+    // 4. dW1 = X^T . dZ (columns block i = shard i)
+    if (dW1) {
+        GemmCall c{};
+        c.A = X; c.a_mn = true; c.B = dZ; c.M = d; c.N = f; c.K = M;
+        c.k_groups = 1; c.out = dW1; c.out_f32 = f32; c.n_shards = 1; c.col_groups = 1;
+        if ((st = launch_gemm(c, s)) != TP_OK) return st;
+    }
+    // 5. dX = dZ . W1^T: the K loop walks the hidden columns, shard 0's first,
+    //    so the shards' contributions are added in ascending order
+    if (dX) {
+        GemmCall c{};
+        c.A = dZ; c.B = W1; c.b_km = true;  // W1 is [d][f] = [N'][K']
+        c.M = M; c.N = d; c.K = f;
+        c.k_groups = 1; c.out = dX; c.out_f32 = f32; c.n_shards = 1; c.col_groups = 1;
+        if ((st = launch_gemm(c, s)) != TP_OK) return st;
+    }
+    return TP_OK;
 }
 
 tp_status tp_get_device_status(cudaStream_t s) {

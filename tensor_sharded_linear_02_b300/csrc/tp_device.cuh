@@ -218,6 +218,15 @@ __device__ __forceinline__ void bulk_wait0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -367,9 +376,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   bit 15 A major (0 = K-major), bit 16 B major (1 = MN-major),
 //   bits 17-22 N >> 3, bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major,
+                                                      bool a_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -439,6 +450,31 @@ __device__ __forceinline__ float gelu_f32(float x) {
     h *= 0.5f;  // erfc(z) / 2
     const float phi = x >= 0.0f ? 1.0f - h : h;
     return x * phi;
+}
+
+// GeLU'(x) = Phi(x) + x * phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi), in fp32:
+// Phi from the same Abramowitz & Stegun 7.1.28 evaluation as gelu_f32, the
+// density from the hardware base-2 exponential (exp(-x^2/2) =
+// 2^(-x^2/2 * log2 e)).
+__device__ __forceinline__ float gelu_grad_f32(float x) {
+    const float z = fabsf(x) * 0.70710678118654752440f;
+    float p = fmaf(4.30638e-5f, z, 2.765672e-4f);
+    p = fmaf(p, z, 1.520143e-4f);
+    p = fmaf(p, z, 9.2705272e-3f);
+    p = fmaf(p, z, 4.22820123e-2f);
+    p = fmaf(p, z, 7.05230784e-2f);
+    p = fmaf(p, z, 1.0f);
+    p = p * p;
+    p = p * p;
+    p = p * p;
+    p = p * p;
+    float h;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
+    h *= 0.5f;  // erfc(|x|/sqrt 2) / 2
+    const float phi_cdf = x >= 0.0f ? 1.0f - h : h;
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * -0.72134752044448170368f));
+    return fmaf(x * 0.39894228040143267794f, e, phi_cdf);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

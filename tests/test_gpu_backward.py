@@ -1,0 +1,165 @@
+"""GPU parity of the backward pass against the fp64 oracle: the sharded
+linears' gradients (bit-exact on integer-valued bf16 inputs, within the
+accuracy bar on normal inputs) and the MLP block's (recomputed
+pre-activation, GeLU' in the epilogue, shard sum of dX in the accumulator).
+The products read X^T and W^T in place through the tensor cores' transposed
+operand layouts; ragged sizes exercise the zero-filled tails of those
+layouts."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import assert_bf16_parity, bf16_dev_to_f64, dev_bits, dev_to_f64, to_dev_bf16
+from tensor_sharded_linear_02_b300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from tensor_sharded_linear_02_b300 import binding
+    binding.lib()
+    return binding
+
+
+def _int_bf16(shape, seed):
+    v = inputs.int_uniform(shape, seed)
+    return oracle.f64_to_bf16(v)
+
+
+@pytest.mark.parametrize("kind", ["column", "row"])
+@pytest.mark.parametrize("M,K,N,n", [(300, 264, 640, 2), (513, 128, 392, 4), (64, 520, 256, 8),
+                                     (1, 8, 8, 1)])
+def test_linear_backward_integer_exact(tp, cuda_device, kind, M, K, N, n):
+    """Integer-valued bf16 inputs in [-4, 4]: every product and partial sum is
+    an integer below 2^24, so the fp32 gradients equal the oracle's exactly."""
+    import torch
+    if (kind == "column" and N % n) or (kind == "row" and K % n):
+        pytest.skip("shard count does not divide the split axis")
+    xb = _int_bf16((M, K), inputs.stream_seed(M + K, 0))
+    wb = _int_bf16((K, N), inputs.stream_seed(M + K, 1))
+    gb = _int_bf16((M, N), inputs.stream_seed(M + K, 2))
+    X, W, dY = (to_dev_bf16(b, cuda_device) for b in (xb, wb, gb))
+    dX = torch.empty(M, K, dtype=torch.float32, device=cuda_device)
+    dW = torch.empty(K, N, dtype=torch.float32, device=cuda_device)
+    fn = tp.tp_column_linear_backward if kind == "column" else tp.tp_row_linear_backward
+    fn(X, W, dY, dX, dW, n_shards=n)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    back = oracle.column_linear_backward if kind == "column" else oracle.row_linear_backward
+    rX, rW = back(*(oracle.bf16_to_f64(b) for b in (xb, wb, gb)), n)
+    np.testing.assert_array_equal(dev_to_f64(dX), rX)
+    np.testing.assert_array_equal(dev_to_f64(dW), rW)
+
+
+@pytest.mark.parametrize("kind", ["column", "row"])
+def test_linear_backward_bf16(tp, cuda_device, kind):
+    """Normal inputs, bf16 and fp32 gradients within the accuracy bar; a
+    NULL output skips that gradient."""
+    import torch
+    M, K, N, n = 700, 512, 1032, 4 if kind == "row" else 2
+    N = 1032 if kind == "row" else 1040
+    xb = inputs.bf16_normal((M, K), inputs.stream_seed(31, 0), 1.0)
+    wb = inputs.bf16_normal((K, N), inputs.stream_seed(31, 1), 0.02)
+    gb = inputs.bf16_normal((M, N), inputs.stream_seed(31, 2), 1.0)
+    X, W, dY = (to_dev_bf16(b, cuda_device) for b in (xb, wb, gb))
+    fn = tp.tp_column_linear_backward if kind == "column" else tp.tp_row_linear_backward
+    back = oracle.column_linear_backward if kind == "column" else oracle.row_linear_backward
+    rX, rW = back(*(oracle.bf16_to_f64(b) for b in (xb, wb, gb)), n)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=cuda_device)
+    dW = torch.empty(K, N, dtype=torch.bfloat16, device=cuda_device)
+    fn(X, W, dY, dX, dW, n_shards=n)
+    dXf = torch.empty(M, K, dtype=torch.float32, device=cuda_device)
+    fn(X, W, dY, dXf, None, n_shards=n)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    assert_bf16_parity(bf16_dev_to_f64(dX), rX, f"{kind} dX")
+    assert_bf16_parity(bf16_dev_to_f64(dW), rW, f"{kind} dW")
+    assert_bf16_parity(dev_to_f64(dXf), rX, f"{kind} dX fp32", out_bf16=False)
+    np.testing.assert_array_equal(dev_bits(dXf.to(torch.bfloat16)), dev_bits(dX))
+
+
+@pytest.mark.parametrize("M,d,f,n", [(200, 256, 512, 2), (300, 264, 1000, 4),
+                                     (2048, 1024, 4096, 2)])
+def test_mlp_block_backward(tp, cuda_device, M, d, f, n):
+    """dX, dW1, dW2 of the MLP block against the oracle (fp64, per shard,
+    pre-activation recomputed exactly); the recomputed H equals the forward
+    pass's H bit for bit; two calls give identical results."""
+    import torch
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(41, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(41, 1), 0.02)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(41, 2), 0.02)
+    gb = inputs.bf16_normal((M, d), inputs.stream_seed(41, 3), 1.0)
+    X, W1, W2, dY = (to_dev_bf16(b, cuda_device) for b in (xb, w1b, w2b, gb))
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=cuda_device)
+    outs = []
+    for _ in range(2):
+        dX = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+        dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=cuda_device)
+        dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=cuda_device)
+        tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+        outs.append((dX, dW1, dW2))
+    assert tp.tp_get_device_status() == tp.TP_OK
+    rX, rW1, rW2 = oracle.mlp_block_backward(*(oracle.bf16_to_f64(b) for b in (xb, w1b, w2b, gb)),
+                                             n)
+    assert_bf16_parity(bf16_dev_to_f64(outs[0][0]), rX, "MLP dX")
+    assert_bf16_parity(bf16_dev_to_f64(outs[0][1]), rW1, "MLP dW1")
+    assert_bf16_parity(bf16_dev_to_f64(outs[0][2]), rW2, "MLP dW2")
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(dev_bits(a), dev_bits(b))
+    # the recomputed H (second part of the workspace) is the forward's H
+    part = (M * f * 2 + 255) // 256 * 256
+    H_bwd = ws[part: part + M * f * 2].view(torch.bfloat16).view(M, f)
+    fws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                      device=cuda_device)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_mlp_block(X, W1, W2, Y, fws, n_shards=n)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    H_fwd = fws[: M * f * 2].view(torch.bfloat16).view(M, f)
+    np.testing.assert_array_equal(dev_bits(H_bwd), dev_bits(H_fwd))
+
+
+def test_mlp_block_backward_fp32_grads_and_skips(tp, cuda_device):
+    """fp32 gradients round to the bf16 ones; NULL outputs are skipped."""
+    import torch
+    M, d, f, n = 256, 128, 384, 3
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(43, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(43, 1), 0.05)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(43, 2), 0.05)
+    gb = inputs.bf16_normal((M, d), inputs.stream_seed(43, 3), 1.0)
+    X, W1, W2, dY = (to_dev_bf16(b, cuda_device) for b in (xb, w1b, w2b, gb))
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=cuda_device)
+    dX = torch.empty(M, d, dtype=torch.float32, device=cuda_device)
+    dW1 = torch.empty(d, f, dtype=torch.float32, device=cuda_device)
+    dW2 = torch.empty(f, d, dtype=torch.float32, device=cuda_device)
+    tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+    dW2_only = torch.full((f, d), float("nan"), dtype=torch.float32, device=cuda_device)
+    tp.tp_mlp_block_backward(X, W1, W2, dY, ws, None, None, dW2_only, n_shards=n)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    rX, rW1, rW2 = oracle.mlp_block_backward(*(oracle.bf16_to_f64(b) for b in (xb, w1b, w2b, gb)),
+                                             n)
+    assert_bf16_parity(dev_to_f64(dX), rX, "dX fp32", out_bf16=False)
+    assert_bf16_parity(dev_to_f64(dW1), rW1, "dW1 fp32", out_bf16=False)
+    assert_bf16_parity(dev_to_f64(dW2), rW2, "dW2 fp32", out_bf16=False)
+    np.testing.assert_array_equal(dev_bits(dW2_only), dev_bits(dW2))
+
+
+def test_backward_validation(tp, cuda_device):
+    import torch
+    X = torch.zeros(16, 24, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.zeros(24, 40, dtype=torch.bfloat16, device=cuda_device)
+    dY = torch.zeros(16, 40, dtype=torch.bfloat16, device=cuda_device)
+    dX = torch.zeros(16, 24, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_column_linear_backward(X, W, dY, dX, None, n_shards=3)  # 3 does not divide 40
+    assert e.value.status == 3
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_row_linear_backward(X, W, dY, dX, None, n_shards=5)     # 5 does not divide 24
+    assert e.value.status == 3
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_column_linear_backward(X, W, dY, X, None, n_shards=2)   # dX aliases X
+    assert e.value.status == 9
+    with pytest.raises(tp.TPError) as e:                              # fp32 inputs
+        tp.tp_column_linear_backward(X.float(), W.float(), dY.float(), dX.float(), None)
+    assert e.value.status == 5
+    assert tp.tp_get_device_status() == tp.TP_OK
