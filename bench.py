@@ -334,6 +334,12 @@ def run_ours(args):
         red["sweep"]["8"] = red["value"]
         cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
 
+    # ----------------------------------------------------------- backward ----
+    bwd = None
+    if not args.skip_extras:
+        bwd = bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks,
+                             K=min(K, 200))
+
     # --------------------------------------------------------------- e2e ----
     Ke = min(K, 500) if not args.skip_extras else 3
     e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
@@ -393,6 +399,7 @@ def run_ours(args):
                                    "gemm_row_shard_sum": round(k2_ms, 5)}},
         "reduce": red,
         "concat": cat,
+        "backward": bwd,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * d * 2,
                 "ms_per_step": round(e2e_ms, 5), "copy_us_alone": copy_us,
@@ -400,7 +407,7 @@ def run_ours(args):
                         "back to pinned host memory; copies on their own streams, double "
                         "buffered, so step i's copies overlap the neighbouring steps' "
                         "kernels; timed from the first copy in to the last copy out"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 2 * K,  # the timed region: two GEMM launches per step
         "cpu_baseline": cpu,
         "clocks": clocks,
         "wall_s_timed_loop": round(t_wall, 3),
@@ -511,6 +518,43 @@ def _profile_traffic(workload, field="bytes"):
     if not entry or entry.get("source_sha") != kernel_source_sha():
         return None
     return entry.get(field)
+
+
+def bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks, K=200):
+    """tp_mlp_block_backward on the bench workload (dY ~ N(0,1) synthetic).
+    Counted work: the four products of the backward pass, 4 * 2*M*d*f (the
+    recomputation of the pre-activation, a fifth product, is not counted)."""
+    from tensor_sharded_linear_02_b300 import inputs
+    dY = _bf16_dev(inputs.bf16_normal((M, d), inputs.stream_seed(1, 3), 1.0), X.device)
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=X.device)
+    dX = torch.empty(M, d, dtype=torch.bfloat16, device=X.device)
+    dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=X.device)
+    dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=X.device)
+
+    def step():
+        tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+
+    for _ in range(5):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        _prequeue(torch, i)
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    flops = 4 * 2.0 * M * d * f
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"MLP block backward, same sizes, N={n}", "value": round(tf, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(ms, 5), "flops_per_step": flops,
+            "launches_per_step": 5, "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "note": "dX, dW1, dW2 (bf16) with the pre-activation recomputed; L2 flushed "
+                    "before every step; counted work excludes the recomputation"}
 
 
 def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
