@@ -88,10 +88,10 @@ def _load():
         lib.orc_bf16_from_double.restype = ctypes.c_uint16
         lib.orc_bf16_to_double_array.argtypes = [_u16p, _dp, _i64]
         lib.orc_double_to_bf16_array.argtypes = [_dp, _u16p, _i64]
-        lib.orc_column_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
+        lib.orc_column_linear.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
                                           _i64, _i64, ctypes.c_int]
-        lib.orc_row_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
-        lib.orc_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
+        lib.orc_row_linear.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
+        lib.orc_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                       ctypes.c_int]
         lib.orc_gelu_grad.argtypes = [ctypes.c_double]
         lib.orc_gelu_grad.restype = ctypes.c_double
@@ -163,50 +163,58 @@ def matmul(X, W) -> np.ndarray:
     return Y
 
 
-def column_linear(X, W, n_shards: int, col_groups: int = 1, act: str | None = None):
+def column_linear(X, W, n_shards: int, col_groups: int = 1, act: str | None = None, bias=None):
     """Column-parallel linear ([TP-topic] "Column-Wise Parallelism").
 
     Returns (Y, Ys): the concatenated output [M, N] and the shard-major local
     outputs [n_shards, M, N/n_shards].  ``act='gelu'`` applies the exact GeLU
-    to each shard's output before the concat.
+    to each shard's output before the concat; ``bias`` [N] is split with W's
+    columns and added by each shard before the activation.
     """
     X, W = _f64(X), _f64(W)
+    b = None if bias is None else _f64(bias)
     M, K = X.shape
     _, N = W.shape
     assert N % col_groups == 0 and (N // col_groups) % n_shards == 0
     Y = np.empty((M, N), dtype=np.float64)
     Ys = np.empty((n_shards, M, N // n_shards), dtype=np.float64)
-    _load().orc_column_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(Ys), M, K, N,
+    _load().orc_column_linear(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), _ptr(Ys), M, K, N,
                               n_shards, col_groups, 1 if act == "gelu" else 0)
     return Y, Ys
 
 
-def row_linear(X, W, n_shards: int):
+def row_linear(X, W, n_shards: int, bias=None):
     """Row-parallel linear ([TP-topic] "Row-Wise Parallelism").
 
-    Returns (Y, P): Y = sum of the shard partials (ascending shard order) and
-    the partials P [n_shards, M, N].
+    Returns (Y, P): Y = sum of the shard partials (ascending shard order),
+    plus ``bias`` [N] once after the sum if given, and the bias-free
+    partials P [n_shards, M, N].
     """
     X, W = _f64(X), _f64(W)
+    b = None if bias is None else _f64(bias)
     M, K = X.shape
     _, N = W.shape
     assert K % n_shards == 0
     Y = np.empty((M, N), dtype=np.float64)
     P = np.empty((n_shards, M, N), dtype=np.float64)
-    _load().orc_row_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(P), M, K, N, n_shards)
+    _load().orc_row_linear(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), _ptr(P), M, K, N, n_shards)
     return Y, P
 
 
-def mlp_block(X, W1, W2, n_shards: int, mirror_h_bf16: bool = False) -> np.ndarray:
+def mlp_block(X, W1, W2, n_shards: int, mirror_h_bf16: bool = False, b1=None,
+              b2=None) -> np.ndarray:
     """Megatron-style MLP block ([TP-topic] Megatron-LM, "MLP Layer Splitting"):
-    Y = sum_i GeLU(X.W1_i).W2_i with W1 split by columns and W2 by rows."""
+    Y = sum_i GeLU(X.W1_i + b1_i).W2_i + b2 with W1 (and b1) split by columns
+    and W2 by rows; b2 is added once after the sum."""
     X, W1, W2 = _f64(X), _f64(W1), _f64(W2)
+    c1 = None if b1 is None else _f64(b1)
+    c2 = None if b2 is None else _f64(b2)
     M, d = X.shape
     _, f = W1.shape
     assert W2.shape == (f, d) and f % n_shards == 0
     Y = np.empty((M, d), dtype=np.float64)
-    _load().orc_mlp_block(_ptr(X), _ptr(W1), _ptr(W2), _ptr(Y), M, d, f, n_shards,
-                          1 if mirror_h_bf16 else 0)
+    _load().orc_mlp_block(_ptr(X), _ptr(W1), _ptr(c1), _ptr(W2), _ptr(c2), _ptr(Y), M, d, f,
+                          n_shards, 1 if mirror_h_bf16 else 0)
     return Y
 
 

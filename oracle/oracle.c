@@ -144,8 +144,8 @@ void orc_double_to_bf16_array(const double *src, uint16_t *dst, int64_t n)
 /* gw = N/G and sw = gw/n, shard i owns columns {b*gw + i*sw + j}, b < G,    */
 /* j < sw, and its local output is [M, G*sw] ordered block by block.         */
 /* ------------------------------------------------------------------------ */
-void orc_column_linear(const double *X, const double *W, double *Y, double *Ys,
-                       int64_t M, int64_t K, int64_t N, int64_t n_shards,
+void orc_column_linear(const double *X, const double *W, const double *bias, double *Y,
+                       double *Ys, int64_t M, int64_t K, int64_t N, int64_t n_shards,
                        int64_t col_groups, int act_gelu)
 {
     const int64_t gw = N / col_groups;
@@ -160,6 +160,11 @@ void orc_column_linear(const double *X, const double *W, double *Y, double *Ys,
                 for (int64_t j = 0; j < sw; ++j)
                     Wi[k * nl + b * sw + j] = W[k * N + b * gw + i * sw + j];
         orc_matmul(X, Wi, Yi, M, K, nl);
+        if (bias)   /* the shard's slice of the bias, before the activation */
+            for (int64_t r = 0; r < M; ++r)
+                for (int64_t b = 0; b < col_groups; ++b)
+                    for (int64_t j = 0; j < sw; ++j)
+                        Yi[r * nl + b * sw + j] += bias[b * gw + i * sw + j];
         if (act_gelu)
             orc_gelu_inplace(Yi, M * nl);       /* per shard, no exchange */
         /* all-gather: place the shard's columns into the full output */
@@ -185,8 +190,8 @@ void orc_column_linear(const double *X, const double *W, double *Y, double *Ys,
 /* The partials are summed in ascending shard order.  P, if given, receives */
 /* the partials as [n, M, N].                                                */
 /* ------------------------------------------------------------------------ */
-void orc_row_linear(const double *X, const double *W, double *Y, double *P,
-                    int64_t M, int64_t K, int64_t N, int64_t n_shards)
+void orc_row_linear(const double *X, const double *W, const double *bias, double *Y,
+                    double *P, int64_t M, int64_t K, int64_t N, int64_t n_shards)
 {
     const int64_t ks = K / n_shards;
     double *Xi = (double *)malloc(sizeof(double) * (size_t)(M * ks > 0 ? M * ks : 1));
@@ -205,6 +210,10 @@ void orc_row_linear(const double *X, const double *W, double *Y, double *P,
         if (P)
             memcpy(P + i * M * N, Pi, sizeof(double) * (size_t)(M * N));
     }
+    if (bias)   /* added once, after the sum of the shards (not per shard) */
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t j = 0; j < N; ++j)
+                Y[r * N + j] += bias[j];
     free(Xi);
     free(Pi);
 }
@@ -218,13 +227,16 @@ void orc_row_linear(const double *X, const double *W, double *Y, double *P,
 /*                                                                           */
 /* X [M,d], W1 [d,f], W2 [f,d].  Shard i: H_i = GeLU(X . W1_i) [M, f/n];     */
 /* P_i = H_i . W2_i with W2_i = rows [i*f/n, (i+1)*f/n) of W2;               */
-/* Y = sum_i P_i (ascending i).                                              */
+/* Y = sum_i P_i (ascending i).  Biases (optional): b1 [f] split with W1's  */
+/* columns and added per shard before the GeLU; b2 [d] added once after the */
+/* sum (a bias per shard would be counted n times).                          */
 /* If mirror_h_bf16 != 0, H_i is rounded to bf16 before the second product  */
 /* (a diagnostic that separates rounding of the hidden activation from       */
 /* other differences; it is not the reference result).                       */
 /* ------------------------------------------------------------------------ */
-void orc_mlp_block(const double *X, const double *W1, const double *W2, double *Y,
-                   int64_t M, int64_t d, int64_t f, int64_t n_shards, int mirror_h_bf16)
+void orc_mlp_block(const double *X, const double *W1, const double *b1, const double *W2,
+                   const double *b2, double *Y, int64_t M, int64_t d, int64_t f,
+                   int64_t n_shards, int mirror_h_bf16)
 {
     const int64_t fs = f / n_shards;
     double *W1i = (double *)malloc(sizeof(double) * (size_t)(d * fs > 0 ? d * fs : 1));
@@ -237,6 +249,10 @@ void orc_mlp_block(const double *X, const double *W1, const double *W2, double *
             for (int64_t j = 0; j < fs; ++j)
                 W1i[k * fs + j] = W1[k * f + i * fs + j];
         orc_matmul(X, W1i, Hi, M, d, fs);
+        if (b1)   /* the shard's slice of the first bias, before the activation */
+            for (int64_t r = 0; r < M; ++r)
+                for (int64_t j = 0; j < fs; ++j)
+                    Hi[r * fs + j] += b1[i * fs + j];
         orc_gelu_inplace(Hi, M * fs);
         if (mirror_h_bf16)
             for (int64_t t = 0; t < M * fs; ++t)
@@ -245,6 +261,10 @@ void orc_mlp_block(const double *X, const double *W1, const double *W2, double *
         for (int64_t t = 0; t < M * d; ++t)
             Y[t] += Pi[t];
     }
+    if (b2)   /* the second bias once, after the sum */
+        for (int64_t r = 0; r < M; ++r)
+            for (int64_t j = 0; j < d; ++j)
+                Y[r * d + j] += b2[j];
     free(W1i);
     free(Hi);
     free(Pi);

@@ -153,6 +153,49 @@ def test_mlp_brute_force_with_library_gelu():
         np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
 
 
+def test_bias_brute_force_integer_shapes():
+    """Biases on tiny integer shapes against plain Python loops: the column
+    split adds each shard's slice of the bias to its outputs, the row split
+    adds the bias once after the sum, for every shard count; a bias added by
+    every shard of the row split (n times) is caught."""
+    rng = random.Random(777)
+    for _ in range(40):
+        M, K, N = rng.randint(1, 6), rng.randint(1, 8), rng.randint(1, 8)
+        X, W = _rand_int_matrix(rng, M, K), _rand_int_matrix(rng, K, N)
+        b = [rng.randint(-4, 4) for _ in range(N)]
+        ref = [[v + b[j] for j, v in enumerate(row)] for row in _bf_matmul(X, W)]
+        for n in _divisors(N):
+            Y, Ys = oracle.column_linear(X, W, n, bias=b)
+            np.testing.assert_array_equal(Y, ref)
+            w = N // n
+            for i in range(n):
+                np.testing.assert_array_equal(Ys[i], [row[i * w:(i + 1) * w] for row in ref])
+        for n in _divisors(K):
+            Y, P = oracle.row_linear(X, W, n, bias=b)
+            np.testing.assert_array_equal(Y, ref)
+            np.testing.assert_array_equal(P.sum(axis=0), np.array(_bf_matmul(X, W), float))
+            if n > 1 and any(b):
+                per_shard = P.sum(axis=0) + n * np.array(b, float)
+                assert not np.array_equal(per_shard, np.array(ref, float))
+
+
+def test_mlp_bias_brute_force_with_library_gelu():
+    """MLP block with b1 (split with W1, before the GeLU) and b2 (once after
+    the sum) against plain loops with scipy's normal CDF."""
+    rng = np.random.default_rng(8)
+    for M, d, f, n in [(3, 4, 8, 2), (2, 5, 6, 3), (4, 3, 4, 4)]:
+        X = rng.standard_normal((M, d))
+        W1, W2 = rng.standard_normal((d, f)), rng.standard_normal((f, d))
+        b1, b2 = rng.standard_normal(f), rng.standard_normal(d)
+        H = [[sum(X[i, k] * W1[k, j] for k in range(d)) + b1[j] for j in range(f)]
+             for i in range(M)]
+        H = [[h * float(scipy.special.ndtr(h)) for h in row] for row in H]
+        Y = [[sum(H[i][k] * W2[k, j] for k in range(f)) + b2[j] for j in range(d)]
+             for i in range(M)]
+        got = oracle.mlp_block(X, W1, W2, n, b1=b1, b2=b2)
+        np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------- sharded == unsharded --------
 
 def test_sharded_equals_unsharded_float():
