@@ -140,6 +140,28 @@ tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out,
                         tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
 
 /*
+ * Biased variants.  The pages write Y = X W throughout and mention biases
+ * only among the parameters a device holds a part of (Manning liveBook
+ * concept page "Tensor parallelism": each device works on part of a linear
+ * layer's weights and biases); the reading taken: a column-split bias b [Nout] is split
+ * with W's columns and each shard adds its slice to its own outputs (before
+ * the activation); a row-split bias is added ONCE, after the shards'
+ * partials are summed -- added by every shard it would be counted n_shards
+ * times.
+ *   bias: device pointer to Nout values of in_t, or NULL (then these are
+ *   exactly tp_column_linear / tp_row_linear); 16-byte aligned for bf16.
+ *   tp_row_linear_bias with P_out: the partials stay bias-free and the bias
+ *   is added by the reduce that forms Y.
+ * Errors: as the unbiased calls; TP_ERR_ALIAS if an output overlaps bias.
+ */
+tp_status tp_column_linear_bias(const void *X, const void *W, const void *bias, void *Y,
+                                void *Y_shards, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                tp_dtype in_t, tp_dtype out_t, tp_act act, cudaStream_t s);
+tp_status tp_row_linear_bias(const void *X, const void *W, const void *bias, void *Y,
+                             float *P_out, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                             tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
  * Either split, chosen by `split` (glossary "Check your understanding":
  * different output coordinates are concatenated, the same coordinates are
  * added).  TP_SPLIT_COLS calls tp_column_linear(X, W, Y, NULL, ...);
@@ -218,6 +240,17 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y,
                        void *ws, size_t ws_bytes,
                        int64_t M, int64_t d, int64_t f, int n_shards,
                        tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
+ * MLP block with biases: Y = sum_i GeLU(X W1_i + b1_i) W2_i + b2, b1 [f]
+ * split with W1's columns (each shard adds its slice before the GeLU), b2
+ * [d] added once after the sum.  b1 or b2 may be NULL.  Otherwise as
+ * tp_mlp_block.
+ */
+tp_status tp_mlp_block_bias(const void *X, const void *W1, const void *b1, const void *W2,
+                            const void *b2, void *Y, void *ws, size_t ws_bytes, int64_t M,
+                            int64_t d, int64_t f, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                            cudaStream_t s);
 
 /*
  * MLP block without a caller-provided workspace.  (No counterpart on the

@@ -54,6 +54,12 @@ SIGNATURES = {
                       _int, _vp], _int),
     "tp_mlp_block_static_ws": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
                                _int),
+    "tp_column_linear_bias": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int,
+                               _vp], _int),
+    "tp_row_linear_bias": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
+                           _int),
+    "tp_mlp_block_bias": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i64, _i64, _i64,
+                           _int, _int, _int, _vp], _int),
     "tp_column_linear_backward": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int,
                                    _vp], _int),
     "tp_row_linear_backward": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
@@ -194,6 +200,34 @@ def tp_mlp_block(X, W1, W2, Y, ws, n_shards=1, stream=None):
                             ws.numel() * ws.element_size(), M, d, f, n_shards,
                             _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
     _check("tp_mlp_block", st)
+
+
+def tp_column_linear_bias(X, W, bias, Y=None, Y_shards=None, n_shards=1, act=None, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    st = lib().tp_column_linear_bias(_ptr(X), _ptr(W), _ptr(bias), _ptr(Y), _ptr(Y_shards), M, K,
+                                     N, n_shards, _dtype_code(X.dtype),
+                                     _dtype_code(_out_dtype(Y, Y_shards)), _act(act),
+                                     _stream(stream))
+    _check("tp_column_linear_bias", st)
+
+
+def tp_row_linear_bias(X, W, bias, Y=None, P_out=None, n_shards=1, stream=None):
+    M, K = X.shape
+    N = W.shape[1]
+    out_t = _dtype_code(Y.dtype) if Y is not None else TP_F32
+    st = lib().tp_row_linear_bias(_ptr(X), _ptr(W), _ptr(bias), _ptr(Y), _ptr(P_out), M, K, N,
+                                  n_shards, _dtype_code(X.dtype), out_t, _stream(stream))
+    _check("tp_row_linear_bias", st)
+
+
+def tp_mlp_block_bias(X, W1, b1, W2, b2, Y, ws, n_shards=1, stream=None):
+    M, d = X.shape
+    f = W1.shape[1]
+    st = lib().tp_mlp_block_bias(_ptr(X), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _ptr(Y),
+                                 _ptr(ws), ws.numel() * ws.element_size(), M, d, f, n_shards,
+                                 _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
+    _check("tp_mlp_block_bias", st)
 
 
 def _grad_dtype(*ts):

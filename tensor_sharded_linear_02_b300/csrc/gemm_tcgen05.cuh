@@ -142,6 +142,8 @@ struct GemmArgs {
     int tma_store;       // 1: the plain output goes through shared memory and TMA
                          //    stores (tensor map tmC); 0: per-thread vector stores
     int epi;             // EPI_PLAIN, EPI_DUAL or EPI_GELU_GRAD (TMA-store path, bf16)
+    const __nv_bfloat16 *bias;  // optional [N]: added to the accumulator before the
+                                // activation (after the whole K range: once per output)
     void *out_shards;    // optional shard-major copy (column split)
     int shard_sw;        // columns a shard owns in each column group
     int shard_gw;        // columns per column group
@@ -154,8 +156,20 @@ struct GemmArgs {
 // one output row (row < M, col < N, col a multiple of 8).  Writes the plain
 // output (k-group g) and, if requested, the shard-major copy.
 // ---------------------------------------------------------------------------
+// Adds bias[col .. col+7] (bf16; col a multiple of 8, col < N) to f.
+__device__ __forceinline__ void add_bias8(const __nv_bfloat16 *bias, int col, float *f) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(bias + col));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        f[2 * h] += __uint_as_float(w[h] << 16);
+        f[2 * h + 1] += __uint_as_float(w[h] & 0xffff0000u);
+    }
+}
+
 __device__ __forceinline__ void store_vec8(const GemmArgs &a, int g, int row, int col,
                                            float (&f)[8]) {
+    if (a.bias) add_bias8(a.bias, col, f);
     if (a.act_gelu) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) f[i] = gelu_f32(f[i]);
@@ -261,10 +275,30 @@ __device__ __forceinline__ void stage_and_store_box(const CUtensorMap *tmC, uint
 // bf16 output: 64-column boxes; fp32 output: 32-column boxes.  The
 // accumulator is released as soon as its last tensor-memory load is done.
 // Rows >= M and columns >= N of a box are clipped by the TMA unit.
+// With a bias (bf16 [N]), bias[col] is added to every row's accumulator
+// before the activation; every lane reads the same bias vectors (broadcast
+// loads), columns >= N are skipped (the TMA store clips them anyway).
+__device__ __forceinline__ void bias_chunk32(const __nv_bfloat16 *bias, int N, int col0,
+                                             uint32_t (&r)[32]) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (col0 + 8 * v < N) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * v + i]);
+            add_bias8(bias, col0 + 8 * v, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r[8 * v + i] = __float_as_uint(f[i]);
+        }
+    }
+}
+
 __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool out_f32, bool gelu,
                                                    uint32_t taddr, uint32_t stg, int row0,
                                                    int col_base, int cofs, int ncols, int g,
-                                                   uint32_t acc_empty_addr) {
+                                                   uint32_t acc_empty_addr,
+                                                   const __nv_bfloat16 *bias = nullptr,
+                                                   int N = 0) {
     if (!out_f32) {
 #pragma unroll 1
         for (int c = 0; c < ncols; c += 64) {
@@ -273,6 +307,10 @@ __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool 
             tmem_ld_32x32b_x32(taddr + cofs + c + 32, r1);
             tmem_ld_wait();
             if (c + 64 >= ncols) release_accumulator(acc_empty_addr);
+            if (bias) {
+                bias_chunk32(bias, N, col_base + cofs + c, r0);
+                bias_chunk32(bias, N, col_base + cofs + c + 32, r1);
+            }
             uint32_t pk[32];
             if (gelu) {
 #pragma unroll
@@ -299,6 +337,7 @@ __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool 
             tmem_ld_32x32b_x32(taddr + cofs + c, r);
             tmem_ld_wait();
             if (c + 32 >= ncols) release_accumulator(acc_empty_addr);
+            if (bias) bias_chunk32(bias, N, col_base + cofs + c, r);
             if (gelu) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gelu_f32(__uint_as_float(r[i])));
@@ -693,7 +732,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 epilogue_dual(&tmC, &tmAux, taddr, stg, row0, nt * bn, cofs, bn / 2, release);
             } else if (a.tma_store) {
                 epilogue_tma_store(&tmC, a.out_f32 != 0, a.act_gelu != 0, taddr, stg, row0,
-                                   nt * bn, cofs, bn / 2, g, release);
+                                   nt * bn, cofs, bn / 2, g, release, a.bias, a.N);
             } else {
                 epilogue_direct(a, taddr, row0 + lane, nt * bn, cofs, bn / 2, g, release);
             }

@@ -40,7 +40,8 @@ constexpr int RED_SMEM_BYTES = RED_STAGES * RED_STAGE_BYTES + 128;
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(RED_THREADS, 1)
     shard_reduce_bulk_kernel(const float *__restrict__ P, void *__restrict__ Y, int64_t total,
-                             int n_shards, int chunk, uint64_t limit_ns) {
+                             int n_shards, int chunk, uint64_t limit_ns,
+                             const __nv_bfloat16 *__restrict__ bias, int64_t cols) {
     extern __shared__ __align__(128) uint8_t red_smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(red_smem + RED_STAGES * RED_STAGE_BYTES);
     uint64_t *empty = full + RED_STAGES;
@@ -120,6 +121,14 @@ __global__ void __launch_bounds__(RED_THREADS, 1)
                     add4(a0, *reinterpret_cast<const float4 *>(q));
                     add4(a1, *reinterpret_cast<const float4 *>(q + 4));
                 }
+                if (bias) {  // once, after the sum; cols % 8 == 0 keeps the 8 in one row
+                    const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(
+                        bias + (e0 + e) % cols));
+                    a0.x += __uint_as_float(bv.x << 16); a0.y += __uint_as_float(bv.x & 0xffff0000u);
+                    a0.z += __uint_as_float(bv.y << 16); a0.w += __uint_as_float(bv.y & 0xffff0000u);
+                    a1.x += __uint_as_float(bv.z << 16); a1.y += __uint_as_float(bv.z & 0xffff0000u);
+                    a1.z += __uint_as_float(bv.w << 16); a1.w += __uint_as_float(bv.w & 0xffff0000u);
+                }
                 if constexpr (OUT_BF16) {
                     const uint4 u = make_uint4(pack_bf16x2(a0.x, a0.y), pack_bf16x2(a0.z, a0.w),
                                                pack_bf16x2(a1.x, a1.y), pack_bf16x2(a1.z, a1.w));
@@ -145,12 +154,14 @@ __global__ void __launch_bounds__(RED_THREADS, 1)
 // same ascending-order fp32 sum, one element per thread.
 template <bool OUT_BF16>
 __global__ void shard_reduce_scalar_kernel(const float *__restrict__ P, void *__restrict__ Y,
-                                           int64_t total, int n_shards) {
+                                           int64_t total, int n_shards,
+                                           const __nv_bfloat16 *__restrict__ bias, int64_t cols) {
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
          t += step) {
         float acc = P[t];
         for (int s = 1; s < n_shards; ++s) acc += P[static_cast<int64_t>(s) * total + t];
+        if (bias) acc += __bfloat162float(bias[t % cols]);
         if constexpr (OUT_BF16)
             static_cast<__nv_bfloat16 *>(Y)[t] = __float2bfloat16_rn(acc);
         else

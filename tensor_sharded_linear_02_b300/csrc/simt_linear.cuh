@@ -25,6 +25,7 @@ struct SimtArgs {
     int64_t k_shards;   // contraction shards (row split); 1 for the column split
     int act_gelu;
     float *partials;    // optional [k_shards, M, N] fp32 partial outputs
+    const void *bias;   // optional [N] (input dtype), added after the shard sum
     int64_t shard_sw, shard_gw, shard_nl;  // shard-major copy layout (column split)
 };
 
@@ -45,6 +46,7 @@ __global__ void simt_linear_kernel(const Tin *__restrict__ X, const Tin *__restr
             if (a.partials) a.partials[(s * a.M + row) * a.N + col] = p;
             y = (s == 0) ? p : y + p;
         }
+        if (a.bias) y += to_f32(static_cast<const Tin *>(a.bias)[col]);
         if (a.act_gelu) y = gelu_f32(y);
         if (Y) from_f32(y, Y + row * a.N + col);
         if (Ys) {

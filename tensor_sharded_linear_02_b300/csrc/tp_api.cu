@@ -248,6 +248,7 @@ struct GemmCall {
     bool b_km = false;         // B stored transposed (K contiguous)
     int epi = EPI_PLAIN;       // EPI_DUAL / EPI_GELU_GRAD use aux (bf16 [M, N])
     void *aux = nullptr;
+    const void *bias = nullptr;  // bf16 [N], added before the activation
 };
 
 // Launch plan of one GEMM: tile width and, for the cluster split kernel,
@@ -364,6 +365,7 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     GemmArgs a{};
     a.tma_store = tma_store ? 1 : 0;
     a.epi = c.epi;
+    a.bias = static_cast<const __nv_bfloat16 *>(c.bias);
     a.M = static_cast<int>(c.M);
     a.N = static_cast<int>(c.N);
     a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
@@ -464,8 +466,9 @@ int reduce_grid(int64_t work_items, int sm_count) {
 
 template <bool BF16>
 tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_count,
-                          cudaStream_t s) {
-    if (total % 8 == 0) {
+                          const void *bias, int64_t cols, cudaStream_t s) {
+    const __nv_bfloat16 *b = static_cast<const __nv_bfloat16 *>(bias);
+    if (total % 8 == 0 && (!bias || cols % 8 == 0)) {
         // bulk-copy pipeline: each stage holds `chunk` elements of every shard
         const int chunk = (RED_STAGE_BYTES / (4 * n)) & ~7;
         const int64_t n_chunks = (total + chunk - 1) / chunk;
@@ -480,21 +483,24 @@ tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, shard_reduce_bulk_kernel<BF16>, P, Y, total, n, chunk,
-                               wait_limit_ns()) != cudaSuccess)
+                               wait_limit_ns(), b, cols) != cudaSuccess)
             return TP_ERR_CUDA;
         return launch_status();
     }
-    shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n);
+    shard_reduce_scalar_kernel<BF16><<<reduce_grid(total, sm_count), 256, 0, s>>>(P, Y, total, n,
+                                                                                  b, cols);
     return launch_status();
 }
 
+// Y = sum_i P_i (+ bias [cols], bf16, once after the sum).
 tp_status launch_reduce(const float *P, void *Y, int64_t total, int n, tp_dtype out_t,
-                        cudaStream_t s) {
+                        cudaStream_t s, const void *bias = nullptr, int64_t cols = 1) {
     DeviceInfo *dev = nullptr;
     tp_status st = device_info(&dev);
     if (st != TP_OK) return st;
-    return out_t == TP_BF16 ? launch_reduce_t<true>(P, Y, total, n, dev->sm_count, s)
-                            : launch_reduce_t<false>(P, Y, total, n, dev->sm_count, s);
+    return out_t == TP_BF16
+               ? launch_reduce_t<true>(P, Y, total, n, dev->sm_count, bias, cols, s)
+               : launch_reduce_t<false>(P, Y, total, n, dev->sm_count, bias, cols, s);
 }
 
 // ------------------------------------------------------- shared validation --
@@ -509,9 +515,9 @@ tp_status check_sizes(int64_t M, int64_t K, int64_t N) {
     return TP_OK;
 }
 
-tp_status column_impl(const void *X, const void *W, void *Y, void *Ys, int64_t M, int64_t K,
-                      int64_t N, int n, int G, tp_dtype in_t, tp_dtype out_t, tp_act act,
-                      cudaStream_t s) {
+tp_status column_impl(const void *X, const void *W, const void *bias, void *Y, void *Ys,
+                      int64_t M, int64_t K, int64_t N, int n, int G, tp_dtype in_t,
+                      tp_dtype out_t, tp_act act, cudaStream_t s) {
     tp_status st = check_sizes(M, K, N);
     if (st != TP_OK) return st;
     if (!valid_dtype(in_t) || !valid_dtype(out_t) || (act != TP_ACT_NONE && act != TP_ACT_GELU))
@@ -521,19 +527,30 @@ tp_status column_impl(const void *X, const void *W, void *Y, void *Ys, int64_t M
     if (!present(X, xb) || !present(W, wb) || (!Y && !Ys && yb > 0)) return TP_ERR_NULL;
     if ((st = check_shards(n)) != TP_OK) return st;
     if (G < 1 || N % G != 0 || (N / G) % n != 0) return TP_ERR_DIVISIBILITY;
+    const size_t bb = N * it;
     if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W, wb) || overlaps(Ys, yb, X, xb) ||
-        overlaps(Ys, yb, W, wb) || overlaps(Y, yb, Ys, yb))
+        overlaps(Ys, yb, W, wb) || overlaps(Y, yb, Ys, yb) || overlaps(Y, yb, bias, bb) ||
+        overlaps(Ys, yb, bias, bb))
         return TP_ERR_ALIAS;
     const int64_t sw = N / G / n;
     if (in_t == TP_BF16) {
-        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(Ys, 16))
+        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(Ys, 16) ||
+            !aligned(bias, 16))
             return TP_ERR_ALIGNMENT;
         if (K % 8 != 0 || N % 8 != 0 || (Ys && sw % 8 != 0)) return TP_ERR_ALIGNMENT;
     } else {
-        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(Ys, ot))
+        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(Ys, ot) ||
+            !aligned(bias, 4))
             return TP_ERR_ALIGNMENT;
     }
     if (M == 0 || N == 0) return TP_OK;
+    if (K == 0 && bias) {  // empty contraction: every output is act(bias)
+        SimtArgs a{};
+        a.M = M; a.K = 0; a.N = N; a.k_shards = 1; a.act_gelu = (act == TP_ACT_GELU);
+        a.partials = nullptr; a.bias = bias;
+        a.shard_gw = N / G; a.shard_sw = sw; a.shard_nl = sw * G;
+        return launch_simt(X, W, Y, Ys, a, in_t, out_t, s);
+    }
     if (K == 0) {  // empty contraction: every output is act(0) = 0
         if (Y && cudaMemsetAsync(Y, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
         if (Ys && cudaMemsetAsync(Ys, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
@@ -547,11 +564,12 @@ tp_status column_impl(const void *X, const void *W, void *Y, void *Ys, int64_t M
         c.gelu = (act == TP_ACT_GELU);
         c.out_shards = Ys; c.n_shards = n; c.col_groups = G;
         c.allow_split = true;
+        c.bias = bias;
         return launch_gemm(c, s);
     }
     SimtArgs a{};
     a.M = M; a.K = K; a.N = N; a.k_shards = 1; a.act_gelu = (act == TP_ACT_GELU);
-    a.partials = nullptr;
+    a.partials = nullptr; a.bias = bias;
     a.shard_gw = N / G; a.shard_sw = sw; a.shard_nl = sw * G;
     return launch_simt(X, W, Y, Ys, a, in_t, out_t, s);
 }
@@ -581,19 +599,30 @@ const char *tp_status_string(tp_status st) {
 tp_status tp_column_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
                            int64_t K, int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
                            tp_act act, cudaStream_t s) {
-    return column_impl(X, W, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
+    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
+}
+
+tp_status tp_column_linear_bias(const void *X, const void *W, const void *bias, void *Y,
+                                void *Y_shards, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                tp_dtype in_t, tp_dtype out_t, tp_act act, cudaStream_t s) {
+    return column_impl(X, W, bias, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
 }
 
 tp_status tp_column_linear_grouped(const void *X, const void *W, void *Y, void *Y_shards,
                                    int64_t M, int64_t K, int64_t Nout, int n_shards,
                                    int col_groups, tp_dtype in_t, tp_dtype out_t, tp_act act,
                                    cudaStream_t s) {
-    return column_impl(X, W, Y, Y_shards, M, K, Nout, n_shards, col_groups, in_t, out_t, act, s);
+    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, col_groups, in_t, out_t,
+                       act, s);
 }
 
-tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int64_t M, int64_t K,
-                        int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
-                        cudaStream_t s) {
+}  // extern "C"
+
+namespace {
+
+tp_status row_impl(const void *X, const void *W, const void *bias, void *Y, float *P_out,
+                   int64_t M, int64_t K, int64_t Nout, int n_shards, tp_dtype in_t,
+                   tp_dtype out_t, cudaStream_t s) {
     tp_status st = check_sizes(M, K, Nout);
     if (st != TP_OK) return st;
     if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
@@ -603,20 +632,31 @@ tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int
     const size_t pb = static_cast<size_t>(n_shards) * M * Nout * 4;
     if (!present(X, xb) || !present(W, wb) || (!Y && !P_out && yb > 0)) return TP_ERR_NULL;
     if (K % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    const size_t bb = Nout * it;
     if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W, wb) || overlaps(P_out, pb, X, xb) ||
-        overlaps(P_out, pb, W, wb) || overlaps(Y, yb, P_out, pb))
+        overlaps(P_out, pb, W, wb) || overlaps(Y, yb, P_out, pb) || overlaps(Y, yb, bias, bb) ||
+        overlaps(P_out, pb, bias, bb))
         return TP_ERR_ALIAS;
     const int64_t Kg = K / n_shards;
     if (in_t == TP_BF16) {
-        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(P_out, 16))
+        if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16) || !aligned(P_out, 16) ||
+            !aligned(bias, 16))
             return TP_ERR_ALIGNMENT;
         if (K % 8 != 0 || Nout % 8 != 0 || (P_out && Kg % 8 != 0)) return TP_ERR_ALIGNMENT;
     } else {
-        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(P_out, 4))
+        if (!aligned(X, 4) || !aligned(W, 4) || !aligned(Y, ot) || !aligned(P_out, 4) ||
+            !aligned(bias, 4))
             return TP_ERR_ALIGNMENT;
     }
     if (P_out && Y && (!aligned(P_out, 16) || !aligned(Y, 16))) return TP_ERR_ALIGNMENT;
     if (M == 0 || Nout == 0) return TP_OK;
+    if (K == 0 && bias) {  // empty contraction: Y = bias on every row, partials 0
+        SimtArgs a{};
+        a.M = M; a.K = 0; a.N = Nout; a.k_shards = n_shards; a.act_gelu = 0;
+        a.partials = P_out; a.bias = bias;
+        a.shard_gw = Nout; a.shard_sw = Nout; a.shard_nl = Nout;
+        return launch_simt(X, W, Y, nullptr, a, in_t, out_t, s);
+    }
     if (K == 0) {
         if (Y && cudaMemsetAsync(Y, 0, yb, s) != cudaSuccess) return TP_ERR_CUDA;
         if (P_out && cudaMemsetAsync(P_out, 0, pb, s) != cudaSuccess) return TP_ERR_CUDA;
@@ -635,7 +675,8 @@ tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int
             c.out_f32 = true;
             c.allow_split = false;
             if ((st = launch_gemm(c, s)) != TP_OK) return st;
-            return Y ? launch_reduce(P_out, Y, M * Nout, n_shards, out_t, s) : TP_OK;
+            // the bias, if any, is added once by the reduce, after the sum
+            return Y ? launch_reduce(P_out, Y, M * Nout, n_shards, out_t, s, bias, Nout) : TP_OK;
         }
         // fused: the K loop walks the shards in ascending order into one
         // fp32 accumulator (or shard groups summed through the cluster)
@@ -644,13 +685,30 @@ tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int
         c.out_group_stride = 0;
         c.out_f32 = (out_t == TP_F32);
         c.allow_split = true;
+        c.bias = bias;  // in the epilogue: after the whole K range, i.e. once
         return launch_gemm(c, s);
     }
     SimtArgs a{};
     a.M = M; a.K = K; a.N = Nout; a.k_shards = n_shards; a.act_gelu = 0;
-    a.partials = P_out;
+    a.partials = P_out; a.bias = bias;
     a.shard_gw = Nout; a.shard_sw = Nout; a.shard_nl = Nout;
     return launch_simt(X, W, Y, nullptr, a, in_t, out_t, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int64_t M, int64_t K,
+                        int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                        cudaStream_t s) {
+    return row_impl(X, W, nullptr, Y, P_out, M, K, Nout, n_shards, in_t, out_t, s);
+}
+
+tp_status tp_row_linear_bias(const void *X, const void *W, const void *bias, void *Y,
+                             float *P_out, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                             tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    return row_impl(X, W, bias, Y, P_out, M, K, Nout, n_shards, in_t, out_t, s);
 }
 
 tp_status tp_sharded_linear(const void *X, const void *W, void *Y, int64_t M, int64_t K,
@@ -753,9 +811,13 @@ size_t tp_mlp_block_workspace_size(int64_t M, int64_t f, tp_dtype t) {
     return (b + 255) & ~static_cast<size_t>(255);
 }
 
-tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, void *ws,
-                       size_t ws_bytes, int64_t M, int64_t d, int64_t f, int n_shards,
-                       tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+}  // extern "C"
+
+namespace {
+
+tp_status mlp_impl(const void *X, const void *W1, const void *b1, const void *W2,
+                   const void *b2, void *Y, void *ws, size_t ws_bytes, int64_t M, int64_t d,
+                   int64_t f, int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
     tp_status st = check_sizes(M, d, f);
     if (st != TP_OK) return st;
     if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
@@ -768,22 +830,25 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, v
     if (f % n_shards != 0) return TP_ERR_DIVISIBILITY;
     const size_t need = tp_mlp_block_workspace_size(M, f, in_t);
     if (need > 0 && (!ws || ws_bytes < need)) return TP_ERR_WORKSPACE;
+    const size_t b1b = f * it, b2b = d * it;
     if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W1, w1b) || overlaps(Y, yb, W2, w2b) ||
         overlaps(Y, yb, ws, hb) || overlaps(ws, hb, X, xb) || overlaps(ws, hb, W1, w1b) ||
-        overlaps(ws, hb, W2, w2b))
+        overlaps(ws, hb, W2, w2b) || overlaps(Y, yb, b1, b1b) || overlaps(Y, yb, b2, b2b) ||
+        overlaps(ws, hb, b1, b1b) || overlaps(ws, hb, b2, b2b))
         return TP_ERR_ALIAS;
     if (in_t == TP_BF16) {
         if (!aligned(X, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(Y, 16) ||
-            !aligned(ws, 16))
+            !aligned(ws, 16) || !aligned(b1, 16) || !aligned(b2, 16))
             return TP_ERR_ALIGNMENT;
         if (d % 8 != 0 || f % 8 != 0) return TP_ERR_ALIGNMENT;
     } else {
         if (!aligned(X, 4) || !aligned(W1, 4) || !aligned(W2, 4) || !aligned(Y, ot) ||
-            !aligned(ws, 4))
+            !aligned(ws, 4) || !aligned(b1, 4) || !aligned(b2, 4))
             return TP_ERR_ALIGNMENT;
     }
     if (M == 0 || d == 0) return TP_OK;
-    if (f == 0) return cudaMemsetAsync(Y, 0, yb, s) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    if (f == 0)  // empty hidden layer: Y = b2 on every row (or 0)
+        return row_impl(nullptr, nullptr, b2, Y, nullptr, M, 0, d, 1, in_t, out_t, s);
 
     if (in_t == TP_BF16) {
         // step 1: H = GeLU(X . W1), column-parallel, H_i = column block i of H
@@ -792,6 +857,7 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, v
         c1.k_groups = 1; c1.out = ws; c1.out_group_stride = 0; c1.out_f32 = false;
         c1.gelu = true; c1.out_shards = nullptr; c1.n_shards = n_shards; c1.col_groups = 1;
         c1.allow_split = true;
+        c1.bias = b1;  // each shard's slice of b1, before the GeLU
         if ((st = launch_gemm(c1, s)) != TP_OK) return st;
         // step 2: Y = sum_i H_i . W2_i, shard partials added in the accumulator
         GemmCall c2{};
@@ -799,16 +865,37 @@ tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, v
         c2.k_groups = 1; c2.out = Y; c2.out_group_stride = 0; c2.out_f32 = (out_t == TP_F32);
         c2.gelu = false; c2.out_shards = nullptr; c2.n_shards = n_shards; c2.col_groups = 1;
         c2.allow_split = true;
+        c2.bias = b2;  // once, after the sum over all shards
         return launch_gemm(c2, s);
     }
     SimtArgs a1{};
     a1.M = M; a1.K = d; a1.N = f; a1.k_shards = 1; a1.act_gelu = 1; a1.partials = nullptr;
+    a1.bias = b1;
     a1.shard_gw = f; a1.shard_sw = f; a1.shard_nl = f;
     if ((st = launch_simt(X, W1, ws, nullptr, a1, TP_F32, TP_F32, s)) != TP_OK) return st;
     SimtArgs a2{};
     a2.M = M; a2.K = f; a2.N = d; a2.k_shards = n_shards; a2.act_gelu = 0; a2.partials = nullptr;
+    a2.bias = b2;
     a2.shard_gw = d; a2.shard_sw = d; a2.shard_nl = d;
     return launch_simt(ws, W2, Y, nullptr, a2, TP_F32, out_t, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, void *ws,
+                       size_t ws_bytes, int64_t M, int64_t d, int64_t f, int n_shards,
+                       tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    return mlp_impl(X, W1, nullptr, W2, nullptr, Y, ws, ws_bytes, M, d, f, n_shards, in_t, out_t,
+                    s);
+}
+
+tp_status tp_mlp_block_bias(const void *X, const void *W1, const void *b1, const void *W2,
+                            const void *b2, void *Y, void *ws, size_t ws_bytes, int64_t M,
+                            int64_t d, int64_t f, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                            cudaStream_t s) {
+    return mlp_impl(X, W1, b1, W2, b2, Y, ws, ws_bytes, M, d, f, n_shards, in_t, out_t, s);
 }
 
 // ----------------------------------------------------------- backward ----

@@ -456,3 +456,99 @@ def test_empty_inputs(tp, cuda_device):
     tp.tp_shard_reduce(P, R)
     _status_ok(tp)
     assert float(Y0.float().abs().sum()) == 0.0
+
+
+# ------------------------------------------------------------------ bias ----
+
+@pytest.mark.parametrize("M,K,N,n", [(300, 328, 640, 2), (1000, 512, 1152, 8), (64, 64, 264, 3)])
+def test_linear_bias_bf16(tp, cuda_device, M, K, N, n):
+    """Column split: each shard adds its slice of the bias before the GeLU;
+    row split: the bias is added once after the sum (fused accumulator,
+    cluster split and per-shard partials + reduce all agree with the oracle)."""
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=13 * N + K)
+    bb = inputs.bf16_normal((N,), inputs.stream_seed(13 * N + K, 5), 0.5)
+    X, W, b = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device), to_dev_bf16(bb, cuda_device)
+    Xd, Wd, bd = oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), oracle.bf16_to_f64(bb)
+    if N % n == 0:
+        Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+        Ys = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+        tp.tp_column_linear_bias(X, W, b, Yc, Ys, n_shards=n, act="gelu")
+        Yc1 = torch.empty_like(Yc)
+        tp.tp_column_linear_bias(X, W, b, Yc1, None, n_shards=n, act="gelu")
+        _status_ok(tp)
+        ref, ref_s = oracle.column_linear(Xd, Wd, n, act="gelu", bias=bd)
+        assert_bf16_parity(bf16_dev_to_f64(Yc), ref, "column + bias")
+        assert_bf16_parity(bf16_dev_to_f64(Ys), ref_s, "column + bias, shard-major")
+        np.testing.assert_array_equal(dev_bits(Yc), dev_bits(Yc1))
+    if K % n == 0:
+        ref, _ = oracle.row_linear(Xd, Wd, n, bias=bd)
+        for plan in ["256", "split2"]:
+            Yr = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+            _with_plan(plan, lambda: tp.tp_row_linear_bias(X, W, b, Yr, None, n_shards=n))
+            _status_ok(tp)
+            assert_bf16_parity(dev_to_f64(Yr), ref, f"row + bias, plan {plan}", out_bf16=False)
+        if (K // n) % 8 == 0:
+            P = torch.empty(n, M, N, dtype=torch.float32, device=cuda_device)
+            Yp = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+            tp.tp_row_linear_bias(X, W, b, Yp, P, n_shards=n)
+            _status_ok(tp)
+            assert_bf16_parity(bf16_dev_to_f64(Yp), ref, "row + bias via partials")
+            _, Pref = oracle.row_linear(Xd, Wd, n)
+            assert_bf16_parity(dev_to_f64(P), Pref, "bias-free partials", out_bf16=False)
+
+
+def test_bias_integer_exact_and_empty(tp, cuda_device):
+    """Integer-valued fp32 and bf16 inputs with an integer bias: exact; an
+    empty contraction (K = 0) gives act(bias) on every row."""
+    import torch
+    M, K, N, n = 40, 64, 48, 4
+    xi = inputs.int_uniform((M, K), inputs.stream_seed(9, 0))
+    wi = inputs.int_uniform((K, N), inputs.stream_seed(9, 1))
+    bi = inputs.int_uniform((N,), inputs.stream_seed(9, 2))
+    ref_c, _ = oracle.column_linear(xi, wi, n, bias=bi)
+    ref_r, _ = oracle.row_linear(xi, wi, n, bias=bi)
+    for dt in ("f32", "bf16"):
+        conv = (lambda a: to_dev_f32(a, cuda_device)) if dt == "f32" else \
+            (lambda a: to_dev_bf16(oracle.f64_to_bf16(a), cuda_device))
+        X, W, b = conv(xi), conv(wi), conv(bi)
+        Yc = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+        Yr = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+        tp.tp_column_linear_bias(X, W, b, Yc, None, n_shards=n)
+        tp.tp_row_linear_bias(X, W, b, Yr, None, n_shards=n)
+        _status_ok(tp)
+        np.testing.assert_array_equal(dev_to_f64(Yc), ref_c)
+        np.testing.assert_array_equal(dev_to_f64(Yr), ref_r)
+    X0 = torch.zeros(M, 0, dtype=torch.bfloat16, device=cuda_device)
+    W0 = torch.zeros(0, N, dtype=torch.bfloat16, device=cuda_device)
+    b = to_dev_bf16(oracle.f64_to_bf16(bi), cuda_device)
+    Y0 = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+    tp.tp_column_linear_bias(X0, W0, b, Y0, None, n_shards=n, act="gelu")
+    _status_ok(tp)
+    # the epilogue GeLU's bound: 1e-6 * max(1, |x|), |x| <= 4 here
+    np.testing.assert_allclose(dev_to_f64(Y0), np.tile(oracle.gelu(bi), (M, 1)), rtol=0,
+                               atol=4e-6)
+
+
+@pytest.mark.parametrize("M,d,f,n", [(200, 256, 512, 2), (2048, 1024, 4096, 2)])
+def test_mlp_block_bias(tp, cuda_device, M, d, f, n):
+    import torch
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(17, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(17, 1), 0.02)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(17, 2), 0.02)
+    b1b = inputs.bf16_normal((f,), inputs.stream_seed(17, 3), 0.5)
+    b2b = inputs.bf16_normal((d,), inputs.stream_seed(17, 4), 0.5)
+    X, W1, W2, b1, b2 = (to_dev_bf16(a, cuda_device) for a in (xb, w1b, w2b, b1b, b2b))
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=cuda_device)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_mlp_block_bias(X, W1, b1, W2, b2, Y, ws, n_shards=n)
+    Yn = torch.empty_like(Y)
+    tp.tp_mlp_block_bias(X, W1, None, W2, None, Yn, ws, n_shards=n)
+    Yp = torch.empty_like(Y)
+    tp.tp_mlp_block(X, W1, W2, Yp, ws, n_shards=n)
+    _status_ok(tp)
+    ref = oracle.mlp_block(*(oracle.bf16_to_f64(a) for a in (xb, w1b, w2b)), n,
+                           b1=oracle.bf16_to_f64(b1b), b2=oracle.bf16_to_f64(b2b))
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "MLP block + biases")
+    np.testing.assert_array_equal(dev_bits(Yn), dev_bits(Yp))
