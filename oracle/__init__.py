@@ -93,6 +93,7 @@ def _load():
         lib.orc_row_linear.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
         lib.orc_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                       ctypes.c_int]
+        lib.orc_qkv_linear.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64, _i64, _i64]
         lib.orc_gelu_grad.argtypes = [ctypes.c_double]
         lib.orc_gelu_grad.restype = ctypes.c_double
         lib.orc_column_linear_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
@@ -180,6 +181,28 @@ def column_linear(X, W, n_shards: int, col_groups: int = 1, act: str | None = No
     Ys = np.empty((n_shards, M, N // n_shards), dtype=np.float64)
     _load().orc_column_linear(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), _ptr(Ys), M, K, N,
                               n_shards, col_groups, 1 if act == "gelu" else 0)
+    return Y, Ys
+
+
+def qkv_kv_heads_per_shard(hq: int, hkv: int, n_shards: int) -> int:
+    """KV heads each shard holds under the GQA split (see qkv_linear)."""
+    assert hq % n_shards == 0 and (hkv % n_shards == 0 or n_shards % hkv == 0)
+    return hkv // n_shards if hkv >= n_shards else 1
+
+
+def qkv_linear(X, W, hq: int, hkv: int, hd: int, n_shards: int):
+    """QKV projection with grouped-query heads ([TP-topic] SVG figure,
+    "Attention Head Parallelism": split Q heads evenly, replicate the shared
+    KV heads).  W = [Wq | Wk | Wv] [K, (hq + 2 hkv) hd].  Returns (Y, Ys): the
+    full projection [M, (hq+2hkv) hd] and the shard-local outputs
+    [n, M, (hq/n + 2 kvs) hd], each ordered Q | K | V."""
+    X, W = _f64(X), _f64(W)
+    M, K = X.shape
+    kvs = qkv_kv_heads_per_shard(hq, hkv, n_shards)
+    assert W.shape == (K, (hq + 2 * hkv) * hd)
+    Y = np.empty((M, (hq + 2 * hkv) * hd))
+    Ys = np.empty((n_shards, M, (hq // n_shards + 2 * kvs) * hd))
+    _load().orc_qkv_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(Ys), M, K, hq, hkv, hd, n_shards)
     return Y, Ys
 
 

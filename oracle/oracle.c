@@ -181,6 +181,46 @@ void orc_column_linear(const double *X, const double *W, const double *bias, dou
 }
 
 /* ------------------------------------------------------------------------ */
+/* QKV projection with grouped-query attention heads ([TP-topic] SVG figure, */
+/* "Attention Head Parallelism": Q heads split evenly across devices, the    */
+/* shared KV heads replicated).  Wqkv = [Wq | Wk | Wv] with hq, hkv, hkv     */
+/* heads of hd columns each.  Shard i owns Q heads [i*hq/n, (i+1)*hq/n);     */
+/* its KV heads are [i*hkv/n, (i+1)*hkv/n) when n divides hkv (split) and    */
+/* the single head floor(i*hkv/n) when hkv divides n (each KV head held by   */
+/* n/hkv shards).  Shard i's local output is [M, (hq/n + 2*kvs)*hd] ordered  */
+/* Q | K | V (kvs = KV heads per shard); Y is the full projection X.Wqkv in  */
+/* Wqkv's column order (the replicated heads appear once).                   */
+/* ------------------------------------------------------------------------ */
+void orc_qkv_linear(const double *X, const double *W, double *Y, double *Ys, int64_t M,
+                    int64_t K, int64_t hq, int64_t hkv, int64_t hd, int64_t n_shards)
+{
+    const int64_t N = (hq + 2 * hkv) * hd;
+    const int64_t qs = hq / n_shards;
+    const int64_t kvs = hkv >= n_shards ? hkv / n_shards : 1;
+    const int64_t nl = (qs + 2 * kvs) * hd;
+    int64_t *cols = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nl > 0 ? nl : 1));
+    double *Wi = (double *)malloc(sizeof(double) * (size_t)(K * nl > 0 ? K * nl : 1));
+    orc_matmul(X, W, Y, M, K, N);
+    for (int64_t i = 0; i < n_shards; ++i) {
+        const int64_t kv0 = hkv >= n_shards ? i * kvs : (i * hkv) / n_shards;
+        int64_t c = 0;
+        for (int64_t h = i * qs; h < (i + 1) * qs; ++h)            /* Q heads */
+            for (int64_t j = 0; j < hd; ++j) cols[c++] = h * hd + j;
+        for (int64_t h = kv0; h < kv0 + kvs; ++h)                  /* K heads */
+            for (int64_t j = 0; j < hd; ++j) cols[c++] = hq * hd + h * hd + j;
+        for (int64_t h = kv0; h < kv0 + kvs; ++h)                  /* V heads */
+            for (int64_t j = 0; j < hd; ++j) cols[c++] = (hq + hkv) * hd + h * hd + j;
+        /* the shard's weight columns, copied out; its output X . W_i */
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t j = 0; j < nl; ++j)
+                Wi[k * nl + j] = W[k * N + cols[j]];
+        orc_matmul(X, Wi, Ys + i * M * nl, M, K, nl);
+    }
+    free(cols);
+    free(Wi);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Row-parallel linear ([TP-topic] "Row-Wise Parallelism": W stacked         */
 /* vertically [W_0; ...; W_{n-1}], X split to match, Y_i = X_i . W_i,       */
 /* Y = sum_i Y_i; [Glossary] "Worked example": splitting the contracted      */

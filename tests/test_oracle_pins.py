@@ -196,6 +196,34 @@ def test_mlp_bias_brute_force_with_library_gelu():
         np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
 
 
+def test_qkv_gqa_brute_force():
+    """GQA split on tiny integer shapes against Python-int loops: shard i's
+    local output is X times its own Q head columns followed by the K and V
+    columns of the KV heads its Q heads use (split when n divides hkv,
+    replicated when hkv divides n); with hkv = hq it equals the head-group
+    split of column_linear (col_groups = 3), and the full output is X.W."""
+    rng = random.Random(99)
+    for hq, hkv, hd, n in [(4, 2, 2, 2), (4, 1, 3, 4), (8, 2, 1, 8), (6, 3, 2, 3), (4, 4, 2, 2),
+                           (8, 4, 2, 2)]:
+        M, K = rng.randint(1, 4), rng.randint(1, 5)
+        N = (hq + 2 * hkv) * hd
+        X, W = _rand_int_matrix(rng, M, K), _rand_int_matrix(rng, K, N)
+        Y, Ys = oracle.qkv_linear(X, W, hq, hkv, hd, n)
+        full = _bf_matmul(X, W)
+        np.testing.assert_array_equal(Y, full)
+        group = hq // hkv  # Q heads per KV head
+        for i in range(n):
+            qh = list(range(i * hq // n, (i + 1) * hq // n))
+            kvh = sorted({h // group for h in qh})   # the KV heads these Q heads read
+            cols = ([h * hd + j for h in qh for j in range(hd)]
+                    + [hq * hd + h * hd + j for h in kvh for j in range(hd)]
+                    + [(hq + hkv) * hd + h * hd + j for h in kvh for j in range(hd)])
+            np.testing.assert_array_equal(Ys[i], [[row[c] for c in cols] for row in full])
+        if hkv == hq:
+            _, Yg = oracle.column_linear(X, W, n, col_groups=3)
+            np.testing.assert_array_equal(Ys, Yg)
+
+
 # --------------------------------------------- sharded == unsharded --------
 
 def test_sharded_equals_unsharded_float():
