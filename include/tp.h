@@ -200,6 +200,32 @@ tp_status tp_shard_concat(const void *Ys, void *Y, int64_t rows, int64_t shard_c
                           int n_shards, tp_dtype t, cudaStream_t s);
 
 /*
+ * QKV projection with grouped-query attention heads (topic page, SVG figure,
+ * "Attention Head Parallelism": split the Q heads evenly, replicate the
+ * shared KV heads).
+ *
+ *   W = [Wq | Wk | Wv] [K, (n_q_heads + 2 n_kv_heads) * head_dim], head h of
+ *   each block in columns [h*head_dim, (h+1)*head_dim) of that block.
+ *   Shard i owns Q heads [i*n_q/n, (i+1)*n_q/n) and the KV heads its Q heads
+ *   read: [i*n_kv/n, (i+1)*n_kv/n) when n divides n_kv (split), the single
+ *   head floor(i*n_kv/n) when n_kv divides n (held by n/n_kv shards).
+ *   Y [M, (n_q + 2 n_kv) * head_dim]: the full projection X W (required;
+ *     the KV heads are computed once, not once per holder).
+ *   Y_shards (optional) [n, M, (n_q/n + 2 kvs) * head_dim], kvs = KV heads
+ *     per shard: shard i's local [Q_i | K_i | V_i], copied from Y with TMA
+ *     boxes (a replicated KV head lands in every shard that holds it);
+ *     head_dim * sizeof(out_t) must be a multiple of 16.
+ * With n_kv_heads == n_q_heads this is tp_column_linear_grouped with
+ * col_groups = 3.  Errors: TP_ERR_SHAPE if n_kv_heads does not divide
+ * n_q_heads or 3*n_shards > 192; TP_ERR_DIVISIBILITY if n does not divide
+ * n_q_heads or neither of n, n_kv_heads divides the other; as
+ * tp_column_linear otherwise.
+ */
+tp_status tp_qkv_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
+                        int64_t K, int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim,
+                        int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s);
+
+/*
  * Concat for the head-group split: shard i's local columns are col_groups
  * blocks of sw = shard_cols/col_groups columns; block b lands at output
  * columns [b*gw + i*sw, b*gw + (i+1)*sw) with gw = n_shards*sw (the inverse

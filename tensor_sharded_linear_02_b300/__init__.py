@@ -9,6 +9,7 @@ __all__ = [
     "tp_column_linear", "tp_column_linear_grouped", "tp_row_linear",
     "tp_shard_reduce", "tp_shard_concat", "tp_shard_concat_grouped",
     "tp_mlp_block", "tp_mlp_block_workspace_size", "tp_mlp_block_static_ws",
+    "tp_qkv_linear",
     "tp_column_linear_bias", "tp_row_linear_bias", "tp_mlp_block_bias",
     "tp_column_linear_backward", "tp_row_linear_backward", "tp_mlp_block_backward",
     "tp_mlp_block_backward_workspace_size",

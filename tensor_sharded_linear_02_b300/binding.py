@@ -54,6 +54,8 @@ SIGNATURES = {
                       _int, _vp], _int),
     "tp_mlp_block_static_ws": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
                                _int),
+    "tp_qkv_linear": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int, _int, _vp],
+                      _int),
     "tp_column_linear_bias": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _int,
                                _vp], _int),
     "tp_row_linear_bias": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp],
@@ -200,6 +202,15 @@ def tp_mlp_block(X, W1, W2, Y, ws, n_shards=1, stream=None):
                             ws.numel() * ws.element_size(), M, d, f, n_shards,
                             _dtype_code(X.dtype), _dtype_code(Y.dtype), _stream(stream))
     _check("tp_mlp_block", st)
+
+
+def tp_qkv_linear(X, W, Y, Y_shards=None, n_q_heads=1, n_kv_heads=1, head_dim=1, n_shards=1,
+                  stream=None):
+    M, K = X.shape
+    st = lib().tp_qkv_linear(_ptr(X), _ptr(W), _ptr(Y), _ptr(Y_shards), M, K, n_q_heads,
+                             n_kv_heads, head_dim, n_shards, _dtype_code(X.dtype),
+                             _dtype_code(Y.dtype), _stream(stream))
+    _check("tp_qkv_linear", st)
 
 
 def tp_column_linear_bias(X, W, bias, Y=None, Y_shards=None, n_shards=1, act=None, stream=None):

@@ -563,12 +563,13 @@ __device__ __forceinline__ bool mma_kblocks(uint8_t *ring, SmemBarriers *bars, i
         const uint64_t so = static_cast<uint64_t>(stage * (R::STAGE_BYTES >> 4));
         const uint64_t da = a_ring + so, db = b_ring + so;
         constexpr int KPB = BK_BOX / UMMA_K;  // K steps per 64-deep box
+        umma_f16_pair(d_tmem, da, db, idesc, kb > kb0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k) {
+        for (int k = 1; k < BK / UMMA_K; ++k) {
             const uint64_t ak = A_MN ? da + 128 * k
                                      : da + (A_BOX_BYTES >> 4) * (k / KPB) + 2 * (k % KPB);
             const uint64_t bk = B_KM ? db + b_box * (k / KPB) + 2 * (k % KPB) : db + 128 * k;
-            umma_f16_pair(d_tmem, ak, bk, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_f16_pair(d_tmem, ak, bk, idesc, 1u);
         }
         umma_commit_pair_mc(smem_u32(&bars->empty[stage]), pair_mask);
         if (++stage == R::STAGES) {
@@ -640,7 +641,7 @@ __device__ __forceinline__ void gemm_teardown(uint32_t tmem_base, uint32_t tmem_
 // ---------------------------------------------------------------------------
 // Persistent kernel: cluster = one pair, grid = 2 x (pairs launched).
 // ---------------------------------------------------------------------------
-template <int MAXBN, bool A_MN = false, bool B_KM = false>
+template <int MAXBN, bool A_MN = false, bool B_KM = false, int EPI = EPI_PLAIN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const CUtensorMap *maps[4] = {&tmA, &tmB, &tmC, &tmAux};
     gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps,
-               a.epi != EPI_PLAIN ? 4 : (a.tma_store ? 3 : 2));
+               EPI != EPI_PLAIN ? 4 : (a.tma_store ? 3 : 2));
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
@@ -724,11 +725,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tmem_base + acc * ACC_STRIDE + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t release = acc_empty_remote + acc * 8;
             const int row0 = mt * PAIR_M + half * BM + q * 32;
-            if (a.epi == EPI_GELU_GRAD) {
+            if constexpr (EPI == EPI_GELU_GRAD) {
                 if (!epilogue_gelu_grad(&tmC, &tmAux, bars, warp - 2, aux_count, taddr, stg, row0,
                                         nt * bn, cofs, bn / 2, release, limit))
                     break;
-            } else if (a.epi == EPI_DUAL) {
+            } else if constexpr (EPI == EPI_DUAL) {
                 epilogue_dual(&tmC, &tmAux, taddr, stg, row0, nt * bn, cofs, bn / 2, release);
             } else if (a.tma_store) {
                 epilogue_tma_store(&tmC, a.out_f32 != 0, a.act_gelu != 0, taddr, stg, row0,

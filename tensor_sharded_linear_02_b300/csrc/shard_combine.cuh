@@ -263,4 +263,88 @@ __global__ void __launch_bounds__(32, 1)
     bulk_wait0();
 }
 
+// Column-segment copy with TMA boxes: the same ring as the concat, driven
+// by a table of segments.  Segment k copies columns [src_col, src_col +
+// width) of slot src_slot of the source (viewed as [slots][rows][cols]) to
+// columns [dst_col, dst_col + width) of slot dst_slot of the destination.
+// A source segment may be copied to several destinations (replication).
+// Used for the shard-local outputs of the grouped-query QKV projection.
+constexpr int SEG_MAX = 192;
+
+struct SegTable {
+    int n_seg;
+    int box_cols, box_rows;
+    int col_boxes;          // sum over segments of width / box_cols
+    int64_t units;          // row blocks * col_boxes
+    uint32_t box_bytes;
+    uint64_t wait_limit_ns;
+    int prefix[SEG_MAX + 1];  // col-box index where segment k starts
+    int src_slot[SEG_MAX], src_col[SEG_MAX], dst_slot[SEG_MAX], dst_col[SEG_MAX];
+};
+
+__device__ __forceinline__ void seg_decode(const SegTable &t, int64_t u, int &k, int &cb, int &r0) {
+    const int64_t rb = u / t.col_boxes;
+    const int c = static_cast<int>(u - rb * t.col_boxes);
+    k = 0;
+    while (t.prefix[k + 1] <= c) ++k;
+    cb = c - t.prefix[k];
+    r0 = static_cast<int>(rb) * t.box_rows;
+}
+
+__global__ void __launch_bounds__(32, 1)
+    segment_copy_tma_kernel(const __grid_constant__ CUtensorMap tmSrc,
+                            const __grid_constant__ CUtensorMap tmDst,
+                            const __grid_constant__ SegTable t) {
+    extern __shared__ __align__(128) uint8_t seg_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(seg_smem + CAT_STAGES * CAT_BOX_BYTES);
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < CAT_STAGES; ++st) mbar_init(smem_u32(&full[st]), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmSrc);
+        tma_prefetch_desc(&tmDst);
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) grid_dep_trigger();
+    grid_dep_wait();
+    if (threadIdx.x != 0) return;
+
+    const int64_t mine = t.units > blockIdx.x ? (t.units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    bool ok = true;
+    int64_t issued = 0, stored = 0;
+    for (int64_t step = 0; step < mine + CAT_LAG && ok; ++step) {
+        if (step < mine) {
+            const int st = static_cast<int>(step % CAT_STAGES);
+            bulk_wait_read_n<CAT_STAGES - 1 - CAT_LAG>();
+            int k, cb, r0;
+            seg_decode(t, blockIdx.x + step * gridDim.x, k, cb, r0);
+            const uint32_t fb = smem_u32(&full[st]);
+            mbar_arrive_expect_tx(fb, t.box_bytes);
+            tma_load_3d(smem_u32(seg_smem + st * CAT_BOX_BYTES), &tmSrc, fb,
+                        t.src_col[k] + cb * t.box_cols, r0, t.src_slot[k]);
+            issued = step + 1;
+        }
+        const int64_t j = step - CAT_LAG;
+        if (j >= 0 && j < mine) {
+            const int st = static_cast<int>(j % CAT_STAGES);
+            if (!mbar_wait_bounded(smem_u32(&full[st]), static_cast<uint32_t>((j / CAT_STAGES) & 1),
+                                   t.wait_limit_ns, &abort_flag, SITE_MMA_FULL)) {
+                ok = false;
+                break;
+            }
+            int k, cb, r0;
+            seg_decode(t, blockIdx.x + j * gridDim.x, k, cb, r0);
+            tma_store_3d(&tmDst, smem_u32(seg_smem + st * CAT_BOX_BYTES),
+                         t.dst_col[k] + cb * t.box_cols, r0, t.dst_slot[k]);
+            bulk_commit_group();
+            stored = j + 1;
+        }
+    }
+    for (int64_t j = stored; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&full[j % CAT_STAGES]),
+                        static_cast<uint32_t>((j / CAT_STAGES) & 1), t.wait_limit_ns);
+    bulk_wait0();
+}
+
 }  // namespace tpk

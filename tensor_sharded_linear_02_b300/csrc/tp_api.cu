@@ -75,6 +75,12 @@ tp_status device_info(DeviceInfo **out) {
             cudaFuncSetAttribute(gemm_persistent_kernel<256, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<256, false, true, EPI_GELU_GRAD>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<256, false, false, EPI_DUAL>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<256>::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(gemm_cluster_sum_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<256>::SMEM_BYTES) != cudaSuccess ||
@@ -85,6 +91,9 @@ tp_status device_info(DeviceInfo **out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  RED_SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(shard_concat_tma_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CAT_SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(segment_copy_tma_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  CAT_SMEM_BYTES) != cudaSuccess)
             return TP_ERR_CUDA;
@@ -419,9 +428,15 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     else if (c.a_mn)
         e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, true, false>, tmA, tmB, tmC,
                                tmAux, a);
+    else if (c.b_km && c.epi == EPI_GELU_GRAD)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, true, EPI_GELU_GRAD>,
+                               tmA, tmB, tmC, tmAux, a);
     else if (c.b_km)
         e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, true>, tmA, tmB, tmC,
                                tmAux, a);
+    else if (c.epi == EPI_DUAL)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, false, EPI_DUAL>, tmA,
+                               tmB, tmC, tmAux, a);
     else if (a.bn == 128)
         e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<128>, tmA, tmB, tmC, tmAux, a);
     else
@@ -798,6 +813,110 @@ tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t
     if (cudaLaunchKernelEx(&cfg, shard_concat_tma_kernel, tmSrc, tmDst, a) != cudaSuccess)
         return TP_ERR_CUDA;
     return launch_status();
+}
+
+}  // extern "C"
+
+namespace {
+
+// Copies the segments of table t (all other fields filled by the caller)
+// from src [src_slots][rows][src_cols] to dst [dst_slots][rows][dst_cols].
+tp_status launch_segment_copy(const void *src, int64_t src_slots, int64_t src_cols, void *dst,
+                              int64_t dst_slots, int64_t dst_cols, int64_t rows, bool f32,
+                              SegTable &t, cudaStream_t s) {
+    DeviceInfo *dev = nullptr;
+    tp_status st = device_info(&dev);
+    if (st != TP_OK) return st;
+    const int64_t es = f32 ? 4 : 2;
+    t.box_rows = static_cast<int>(CAT_BOX_BYTES / (t.box_cols * es));
+    if (t.box_rows > 256) t.box_rows = 256;
+    t.units = (rows + t.box_rows - 1) / t.box_rows * t.col_boxes;
+    t.box_bytes = static_cast<uint32_t>(t.box_cols * t.box_rows * es);
+    t.wait_limit_ns = wait_limit_ns();
+    CUtensorMap tmSrc, tmDst;
+    if (!encode_3d_cached(&tmSrc, src, src_cols, rows, src_slots, src_cols * es,
+                          rows * src_cols * es, static_cast<uint32_t>(t.box_cols),
+                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_3d_cached(&tmDst, dst, dst_cols, rows, dst_slots, dst_cols * es,
+                          rows * dst_cols * es, static_cast<uint32_t>(t.box_cols),
+                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return TP_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    const int64_t grid = t.units < dev->sm_count ? t.units : dev->sm_count;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.dynamicSmemBytes = CAT_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, segment_copy_tma_kernel, tmSrc, tmDst, t) != cudaSuccess)
+        return TP_ERR_CUDA;
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_qkv_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
+                        int64_t K, int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim,
+                        int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    if (n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return TP_ERR_SHAPE;
+    if (n_q_heads % n_kv_heads != 0) return TP_ERR_SHAPE;
+    tp_status st = check_shards(n_shards);
+    if (st != TP_OK) return st;
+    if (n_q_heads % n_shards != 0 ||
+        (n_kv_heads % n_shards != 0 && n_shards % n_kv_heads != 0))
+        return TP_ERR_DIVISIBILITY;
+    if (!Y) return TP_ERR_NULL;
+    const int64_t N = (n_q_heads + 2 * n_kv_heads) * head_dim;
+    const int64_t qs = n_q_heads / n_shards;
+    const int64_t kvs = n_kv_heads >= n_shards ? n_kv_heads / n_shards : 1;
+    const int64_t nl = (qs + 2 * kvs) * head_dim;
+    const int64_t es = static_cast<int64_t>(dtype_size(out_t));
+    if (!valid_dtype(out_t)) return TP_ERR_DTYPE;
+    if (Y_shards && (head_dim * es) % 16 != 0) return TP_ERR_ALIGNMENT;
+    if (overlaps(Y_shards, static_cast<size_t>(n_shards) * M * nl * es, Y, M * N * es))
+        return TP_ERR_ALIAS;
+    if (3 * n_shards > SEG_MAX) return TP_ERR_SHAPE;
+    // the full projection in Wqkv's column order (KV heads computed once)
+    if ((st = column_impl(X, W, nullptr, Y, nullptr, M, K, N, 1, 1, in_t, out_t, TP_ACT_NONE,
+                          s)) != TP_OK)
+        return st;
+    if (!Y_shards || M == 0) return TP_OK;
+    if (overlaps(Y_shards, static_cast<size_t>(n_shards) * M * nl * es, X, M * K * dtype_size(in_t)) ||
+        overlaps(Y_shards, static_cast<size_t>(n_shards) * M * nl * es, W, K * N * dtype_size(in_t)))
+        return TP_ERR_ALIAS;
+    if (!aligned(Y_shards, 16)) return TP_ERR_ALIGNMENT;
+    // each shard's Q heads, then the K and V heads its Q heads read
+    SegTable t;
+    std::memset(&t, 0, sizeof(t));
+    int box = 256;
+    while (box > 16 / es && head_dim % box != 0) box /= 2;
+    t.box_cols = box;
+    int nseg = 0, boxes = 0;
+    auto add = [&](int64_t src_col, int64_t dst_slot, int64_t dst_col, int64_t width) {
+        t.prefix[nseg] = boxes;
+        t.src_slot[nseg] = 0;
+        t.src_col[nseg] = static_cast<int>(src_col);
+        t.dst_slot[nseg] = static_cast<int>(dst_slot);
+        t.dst_col[nseg] = static_cast<int>(dst_col);
+        boxes += static_cast<int>(width / box);
+        ++nseg;
+    };
+    for (int64_t i = 0; i < n_shards; ++i) {
+        const int64_t kv0 = n_kv_heads >= n_shards ? i * kvs : (i * n_kv_heads) / n_shards;
+        add(i * qs * head_dim, i, 0, qs * head_dim);
+        add((n_q_heads + kv0) * head_dim, i, qs * head_dim, kvs * head_dim);
+        add((n_q_heads + n_kv_heads + kv0) * head_dim, i, (qs + kvs) * head_dim, kvs * head_dim);
+    }
+    t.prefix[nseg] = boxes;
+    t.n_seg = nseg;
+    t.col_boxes = boxes;
+    return launch_segment_copy(Y, 1, N, Y_shards, n_shards, nl, M, out_t == TP_F32, t, s);
 }
 
 tp_status tp_shard_concat(const void *Ys, void *Y, int64_t rows, int64_t shard_cols,

@@ -552,3 +552,61 @@ def test_mlp_block_bias(tp, cuda_device, M, d, f, n):
                            b1=oracle.bf16_to_f64(b1b), b2=oracle.bf16_to_f64(b2b))
     assert_bf16_parity(bf16_dev_to_f64(Y), ref, "MLP block + biases")
     np.testing.assert_array_equal(dev_bits(Yn), dev_bits(Yp))
+
+
+# ------------------------------------------------------- GQA head split ----
+
+@pytest.mark.parametrize("M,K,hq,hkv,hd,n", [
+    (300, 256, 32, 8, 128, 8),   # KV heads split: one per shard
+    (257, 128, 32, 4, 128, 8),   # KV heads replicated on 2 shards each
+    (64, 64, 16, 1, 64, 4),      # multi-query: one KV head on every shard
+    (100, 64, 8, 8, 64, 4),      # hkv = hq: the head-group split
+])
+def test_qkv_gqa(tp, cuda_device, M, K, hq, hkv, hd, n):
+    """QKV projection with grouped-query heads: the full output against the
+    oracle, each shard's [Q_i | K_i | V_i] bit-equal to the matching columns
+    of the full output (replicated KV heads in every shard that holds them)
+    and within the accuracy bar of the oracle's shard-local products."""
+    import torch
+    N = (hq + 2 * hkv) * hd
+    xb, wb = _bf16_inputs(M, K, N, seed=M + hq + hkv)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    kvs = oracle.qkv_kv_heads_per_shard(hq, hkv, n)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Ys = torch.empty(n, M, (hq // n + 2 * kvs) * hd, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_qkv_linear(X, W, Y, Ys, n_q_heads=hq, n_kv_heads=hkv, head_dim=hd, n_shards=n)
+    _status_ok(tp)
+    ref, ref_s = oracle.qkv_linear(oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), hq, hkv, hd, n)
+    assert_bf16_parity(bf16_dev_to_f64(Y), ref, "QKV full")
+    assert_bf16_parity(bf16_dev_to_f64(Ys), ref_s, "QKV shard-local")
+    # the shard-local outputs are copies of the full output's columns
+    y = dev_bits(Y)
+    ys = dev_bits(Ys)
+    qs = hq // n
+    for i in range(n):
+        kv0 = i * kvs if hkv >= n else (i * hkv) // n
+        cols = (list(range(i * qs * hd, (i + 1) * qs * hd))
+                + list(range((hq + kv0) * hd, (hq + kv0 + kvs) * hd))
+                + list(range((hq + hkv + kv0) * hd, (hq + hkv + kv0 + kvs) * hd)))
+        np.testing.assert_array_equal(ys[i], y[:, cols])
+    if hkv == hq:
+        Yg = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+        tp.tp_column_linear_grouped(X, W, None, Yg, n_shards=n, col_groups=3)
+        _status_ok(tp)
+        np.testing.assert_array_equal(dev_bits(Yg), ys)
+
+
+def test_qkv_gqa_validation(tp, cuda_device):
+    import torch
+    X = torch.zeros(8, 64, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.zeros(64, (8 + 2 * 3) * 64, dtype=torch.bfloat16, device=cuda_device)
+    Y = torch.zeros(8, (8 + 2 * 3) * 64, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(tp.TPError) as e:   # 3 KV heads do not divide 8 Q heads
+        tp.tp_qkv_linear(X, W, Y, None, n_q_heads=8, n_kv_heads=3, head_dim=64, n_shards=2)
+    assert e.value.status == 2
+    W2 = torch.zeros(64, (8 + 2 * 2) * 64, dtype=torch.bfloat16, device=cuda_device)
+    Y2 = torch.zeros(8, (8 + 2 * 2) * 64, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(tp.TPError) as e:   # 3 shards do not divide 8 Q heads
+        tp.tp_qkv_linear(X, W2, Y2, None, n_q_heads=8, n_kv_heads=2, head_dim=64, n_shards=3)
+    assert e.value.status == 3
+    assert tp.tp_get_device_status() == tp.TP_OK
