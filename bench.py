@@ -340,6 +340,11 @@ def run_ours(args):
         bwd = bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks,
                              K=min(K, 200))
 
+    # ------------------------------------------------- the other workloads ----
+    others = None
+    if not args.skip_extras:
+        others = bench_other_workloads(tp, torch, dev, stream, flush, peaks, K=min(K, 20))
+
     # --------------------------------------------------------------- e2e ----
     Ke = min(K, 500) if not args.skip_extras else 3
     e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
@@ -366,12 +371,16 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and not args.skip_extras and world == 1:
-        import oracle
+        # the oracle as it stands, on the whole workload, repeated until about
+        # 10 s of host time have passed
         flops_s, times = cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)
-        cpu = {"value": flops_s / min(times) / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
+        while sum(times) < 10.0:
+            times += cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)[1]
+        mean = sum(times) / len(times)
+        cpu = {"value": flops_s / mean / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
                "kind": "oracle",
-               "sample": f"full workload ({M} rows), fp64 naive loops, 1 pass, "
-                         f"{min(times):.2f} s"}
+               "sample": f"full workload ({M} rows), fp64 naive loops, {len(times)} passes, "
+                         f"{sum(times):.1f} s, mean {mean:.2f} s per pass"}
 
     clocks = clk.summary()
     line = {
@@ -400,6 +409,7 @@ def run_ours(args):
         "reduce": red,
         "concat": cat,
         "backward": bwd,
+        "other_workloads": others,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": M * d * 2, "d2h_bytes_per_step": M * d * 2,
                 "ms_per_step": round(e2e_ms, 5), "copy_us_alone": copy_us,
@@ -557,6 +567,86 @@ def bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks, K=200
                     "before every step; counted work excludes the recomputation"}
 
 
+def _time_steps(torch, step, flush, stream, K):
+    """Mean device time (ms) of K steps, L2 flushed before each, host work
+    pre-queued as in the main loop."""
+    for _ in range(3):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        _prequeue(torch, i)
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / K
+
+
+def bench_other_workloads(tp, torch, dev, stream, flush, peaks, K=20):
+    """The remaining workloads of the method at their stated sizes (inputs
+    from a seeded device generator, same distributions; timing only -- their
+    parity is in the GPU tests): GPT MLP block N = 8, the attention
+    projections (QKV split by head groups, output projection split by rows,
+    N = 8) and the wide MLP block for N = 1, 2, 4, 8, 16."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(20261202)
+
+    def bf(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    peak = peaks["bf16_tflops"]
+    out = {}
+
+    def entry(ms, flops, **kw):
+        tf = flops / (ms * 1e-3) / 1e12
+        return dict(ms_per_step=round(ms, 4), tflops=round(tf, 1), frac_of_peak=round(tf / peak, 4),
+                    **kw)
+
+    M, d, f, n = 4096, 4096, 16384, 8
+    X, W1, W2 = bf(M, d), bf(d, f, std=0.02), bf(f, d, std=0.02)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    ms = _time_steps(torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush,
+                     stream, K)
+    out["mlp_4096x4096x16384_n8"] = entry(ms, 4.0 * M * d * f)
+    del X, W1, W2, Y, ws
+
+    M, d, n = 8192, 4096, 8
+    X, Wqkv, C, Wo = bf(M, d), bf(d, 3 * d, std=0.02), bf(M, d), bf(d, d, std=0.02)
+    Yqkv = torch.empty(M, 3 * d, dtype=torch.bfloat16, device=dev)
+    Yo = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+
+    def attn():
+        tp.tp_column_linear_grouped(X, Wqkv, Yqkv, None, n_shards=n, col_groups=3)
+        tp.tp_row_linear(C, Wo, Yo, None, n_shards=n)
+
+    ms = _time_steps(torch, attn, flush, stream, K)
+    out["attention_projections_8192x4096_n8"] = entry(ms, 2.0 * M * d * 3 * d + 2.0 * M * d * d,
+                                                      note="QKV (32 heads, 8 groups) + Wo")
+    del X, Wqkv, C, Wo, Yqkv, Yo
+
+    M, d, f = 4096, 8192, 28672
+    X, W1, W2 = bf(M, d), bf(d, f, std=0.01), bf(f, d, std=0.01)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    sweep = {}
+    for n in (1, 2, 4, 8, 16):
+        ms = _time_steps(torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush,
+                         stream, max(3, K // 2))
+        sweep[str(n)] = entry(ms, 4.0 * M * d * f)
+    out["mlp_4096x8192x28672_sweep_n"] = sweep
+    del X, W1, W2, Y, ws
+    torch.cuda.synchronize()
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the other workloads")
+    return out
+
+
 def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
     import torch
     from tensor_sharded_linear_02_b300 import inputs
@@ -624,8 +714,14 @@ def run_leg(args):
     K = max(1, args.steps)
     if args.leg == "reduce":
         bench_reduce(tp, dev, stream, peaks, K=K)
-    else:
+    elif args.leg == "concat":
         bench_concat(tp, dev, stream, peaks, K=K)
+    else:
+        M, d, f, n, std = WORKLOADS[args.workload]
+        xb, w1b, w2b = _make_mlp_inputs(M, d, f, std, dev)
+        X, W1, W2 = _bf16_dev(xb, dev), _bf16_dev(w1b, dev), _bf16_dev(w2b, dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks, K=K)
     torch.cuda.synchronize()
     if tp.tp_get_device_status() != tp.TP_OK:
         raise RuntimeError("device status error")
@@ -688,7 +784,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--leg", choices=["reduce", "concat"], default=None,
+    ap.add_argument("--leg", choices=["reduce", "concat", "backward"], default=None,
                     help="run only a few launches of one standalone kernel at its bench "
                          "workload and print nothing else (for profiler captures)")
     ap.add_argument("--skip-extras", action="store_true",

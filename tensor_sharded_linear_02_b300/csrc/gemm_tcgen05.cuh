@@ -109,7 +109,6 @@ struct SmemBarriers {
     uint64_t empty[MAX_STAGES];  // both CTAs: stage consumed (multicast commit)
     uint64_t acc_full[2];        // both CTAs: accumulator ready (multicast commit)
     uint64_t acc_empty[2];       // even CTA: epilogue warps of both CTAs done
-    uint64_t aux_full[EPI_WARPS];  // per epilogue warp: an auxiliary input box landed
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
@@ -119,7 +118,7 @@ static_assert(sizeof(SmemBarriers) <= 256, "barrier block");
 // Epilogue modes of the TMA-store path (bf16 outputs):
 //   EPI_PLAIN      out = act(acc)                      -> tmC
 //   EPI_DUAL       out = acc -> tmC, and GeLU(acc)      -> tmAux
-//   EPI_GELU_GRAD  out = acc * GeLU'(z), z read from tmAux (same shape as out)
+//   EPI_GELU_GRAD  out = acc * GeLU'(z), z (bf16 [M, N]) read from global memory
 enum EpiMode : int { EPI_PLAIN = 0, EPI_DUAL = 1, EPI_GELU_GRAD = 2 };
 
 // Bytes both CTAs of a pair land per k-block of a bn-wide tile.
@@ -144,6 +143,7 @@ struct GemmArgs {
     int epi;             // EPI_PLAIN, EPI_DUAL or EPI_GELU_GRAD (TMA-store path, bf16)
     const __nv_bfloat16 *bias;  // optional [N]: added to the accumulator before the
                                 // activation (after the whole K range: once per output)
+    const __nv_bfloat16 *aux;   // EPI_GELU_GRAD: z, bf16 [M, N]
     void *out_shards;    // optional shard-major copy (column split)
     int shard_sw;        // columns a shard owns in each column group
     int shard_gw;        // columns per column group
@@ -377,47 +377,40 @@ __device__ __forceinline__ void epilogue_dual(const CUtensorMap *tmC, const CUte
     }
 }
 
-// GeLU-gradient epilogue (bf16): out = acc * GeLU'(z).  For each 64-column
-// box, lane 0 loads the matching box of z (bf16, same swizzled 32 x 128-byte
-// layout as the store box) into the warp's store buffer with TMA, counted on
-// the warp's aux barrier; each lane then reads its own row of z, multiplies,
-// and writes the result over it, and the box leaves with one TMA store.
-// `aux_count` counts the boxes this warp has loaded (the barrier's phase).
-__device__ __forceinline__ bool epilogue_gelu_grad(const CUtensorMap *tmC,
-                                                   const CUtensorMap *tmAux, SmemBarriers *bars,
-                                                   int ew, uint32_t &aux_count, uint32_t taddr,
-                                                   uint32_t stg, int row0, int col_base, int cofs,
-                                                   int ncols, uint32_t acc_empty_addr,
-                                                   uint64_t limit) {
+// GeLU-gradient epilogue (bf16): out = acc * GeLU'(z), z (bf16 [M, N]) read
+// from global memory by each lane for its own row (8 read-only 16-byte
+// loads per 64-column box, issued before the tensor-memory loads so that
+// their latency overlaps them; rows >= M and columns >= N read as 0).
+__device__ __forceinline__ void epilogue_gelu_grad(const CUtensorMap *tmC,
+                                                   const __nv_bfloat16 *z, int M, int N,
+                                                   uint32_t taddr, uint32_t stg, int row0,
+                                                   int col_base, int cofs, int ncols,
+                                                   uint32_t acc_empty_addr) {
     const int lane = threadIdx.x & 31;
-    const uint32_t bar = smem_u32(&bars->aux_full[ew]);
+    const int row = row0 + lane;
 #pragma unroll 1
     for (int c = 0; c < ncols; c += 64) {
         const int col = col_base + cofs + c;
-        if (lane == 0) {
-            bulk_wait_read0();  // the previous box has left the buffer
-            mbar_arrive_expect_tx(bar, STG_BYTES);
-            tma_load_3d(stg, tmAux, bar, col, row0, 0);
+        uint4 zv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            zv[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (row < M && col + 8 * q < N)
+                zv[q] = __ldg(reinterpret_cast<const uint4 *>(z + static_cast<int64_t>(row) * N +
+                                                              col + 8 * q));
         }
-        __syncwarp();
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(taddr + cofs + c, r0);
         tmem_ld_32x32b_x32(taddr + cofs + c + 32, r1);
         tmem_ld_wait();
         if (c + 64 >= ncols) release_accumulator(acc_empty_addr);
-        const bool ok = mbar_wait_warp(bar, aux_count & 1u, limit, &bars->abort,
-                                       SITE_EPI_ACC_FULL);
-        ++aux_count;
-        if (!ok) return false;
         uint32_t pk[32];
-        const uint32_t row_addr = stg + lane * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 16-byte chunk q = columns 8q .. 8q+7
-            const uint4 zv = ld_shared_v4(row_addr + ((q ^ (lane & 7)) << 4));
-            const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+        for (int q = 0; q < 8; ++q) {  // columns 8q .. 8q+7 of the box
+            const uint32_t zw[4] = {zv[q].x, zv[q].y, zv[q].z, zv[q].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const int i = 8 * q + 2 * h;  // column within the box
+                const int i = 8 * q + 2 * h;
                 const float z0 = __uint_as_float(zw[h] << 16);
                 const float z1 = __uint_as_float(zw[h] & 0xffff0000u);
                 const float a0 = __uint_as_float(i < 32 ? r0[i] : r1[i - 32]);
@@ -427,7 +420,6 @@ __device__ __forceinline__ bool epilogue_gelu_grad(const CUtensorMap *tmC,
         }
         stage_and_store_box(tmC, stg, pk, col, row0, 0);
     }
-    return true;
 }
 
 __device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_tile, int &n_tile,
@@ -606,7 +598,6 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, int stages, uint3
             mbar_init(smem_u32(&bars->acc_full[i]), 1);
             mbar_init(smem_u32(&bars->acc_empty[i]), 2 * EPI_WARPS);
         }
-        for (int i = 0; i < EPI_WARPS; ++i) mbar_init(smem_u32(&bars->aux_full[i]), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -663,7 +654,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const CUtensorMap *maps[4] = {&tmA, &tmB, &tmC, &tmAux};
     gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps,
-               EPI != EPI_PLAIN ? 4 : (a.tma_store ? 3 : 2));
+               EPI == EPI_DUAL ? 4 : (a.tma_store ? 3 : 2));
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
@@ -710,7 +701,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int cofs = ((warp - 2) >> 2) * (bn / 2);  // this warp's half of the columns
         const uint32_t acc_empty_remote = dsmem_map(smem_u32(&bars->acc_empty[0]), 0);
         const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
-        uint32_t aux_count = 0;
         int local = 0;
         for (int u = pair; u < a.num_units; u += num_pairs, ++local) {
             const int acc = local & 1;
@@ -726,9 +716,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t release = acc_empty_remote + acc * 8;
             const int row0 = mt * PAIR_M + half * BM + q * 32;
             if constexpr (EPI == EPI_GELU_GRAD) {
-                if (!epilogue_gelu_grad(&tmC, &tmAux, bars, warp - 2, aux_count, taddr, stg, row0,
-                                        nt * bn, cofs, bn / 2, release, limit))
-                    break;
+                epilogue_gelu_grad(&tmC, a.aux, a.M, a.N, taddr, stg, row0, nt * bn, cofs, bn / 2,
+                                   release);
             } else if constexpr (EPI == EPI_DUAL) {
                 epilogue_dual(&tmC, &tmAux, taddr, stg, row0, nt * bn, cofs, bn / 2, release);
             } else if (a.tma_store) {

@@ -75,6 +75,9 @@ tp_status device_info(DeviceInfo **out) {
             cudaFuncSetAttribute(gemm_persistent_kernel<256, false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<256>::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_persistent_kernel<128, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Ring<128>::SMEM_BYTES) != cudaSuccess ||
             cudaFuncSetAttribute(gemm_persistent_kernel<256, false, true, EPI_GELU_GRAD>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Ring<256>::SMEM_BYTES) != cudaSuccess ||
@@ -331,7 +334,12 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     if (st != TP_OK) return st;
 
     const int64_t Kg = c.K / c.k_groups;
-    const bool plain = !c.a_mn && !c.b_km && c.epi == EPI_PLAIN;
+    // plans: the K-major-B product (input gradients) may also be 128 wide;
+    // transposed A and the dual / GeLU' epilogues use 256-wide tiles
+    const bool plain = !c.a_mn && c.epi == EPI_PLAIN;
+    const GemmPlan plan = plain ? plan_gemm(c.M, c.N, static_cast<int>((Kg + BK - 1) / BK),
+                                            c.k_groups, c.allow_split && !c.b_km, c.gelu, *dev)
+                                : GemmPlan{256, 1};
     CUtensorMap tmA, tmB, tmAux;
     if (c.a_mn) {
         // A^T stored [K][M]: viewed as [1][K][M]; box = 128 k-rows x 64 columns.
@@ -343,8 +351,9 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
             return TP_ERR_CUDA;
     }
     if (c.b_km) {
-        // B^T stored [N][K]: viewed as [1][N][K]; box = 128 rows x 64 k.
-        if (!encode_3d_cached(&tmB, c.B, c.K, c.N, 1, c.K * 2, c.N * c.K * 2, BK_BOX, 128, 1))
+        // B^T stored [N][K]: viewed as [1][N][K]; box = bn/2 rows x 64 k.
+        if (!encode_3d_cached(&tmB, c.B, c.K, c.N, 1, c.K * 2, c.N * c.K * 2, BK_BOX,
+                              static_cast<uint32_t>(plan.bn / 2), 1))
             return TP_ERR_CUDA;
     } else {
         // B viewed as [k_groups][Kg][N]; box = 128 k-rows x 64 columns of one group.
@@ -353,8 +362,8 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
             return TP_ERR_CUDA;
     }
     std::memset(&tmAux, 0, sizeof(tmAux));
-    if (c.epi != EPI_PLAIN) {
-        // auxiliary bf16 [M, N], same boxes as the bf16 output
+    if (c.epi == EPI_DUAL) {
+        // second bf16 output [M, N], same boxes as the first
         if (!encode_3d_cached(&tmAux, c.aux, c.N, c.M, 1, c.N * 2, c.M * c.N * 2, 64, 32, 1))
             return TP_ERR_CUDA;
     }
@@ -375,14 +384,11 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.tma_store = tma_store ? 1 : 0;
     a.epi = c.epi;
     a.bias = static_cast<const __nv_bfloat16 *>(c.bias);
+    a.aux = static_cast<const __nv_bfloat16 *>(c.aux);
     a.M = static_cast<int>(c.M);
     a.N = static_cast<int>(c.N);
     a.k_blocks = static_cast<int>((Kg + BK - 1) / BK);
     a.k_groups = c.k_groups;
-    // transposed operands and the extra epilogues: persistent, 256 wide
-    const GemmPlan plan = plain ? plan_gemm(c.M, c.N, a.k_blocks, c.k_groups, c.allow_split,
-                                            c.gelu, *dev)
-                                : GemmPlan{256, 1};
     a.bn = plan.bn;
     a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
     a.n_tiles = static_cast<int>((c.N + a.bn - 1) / a.bn);
@@ -431,6 +437,9 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     else if (c.b_km && c.epi == EPI_GELU_GRAD)
         e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, true, EPI_GELU_GRAD>,
                                tmA, tmB, tmC, tmAux, a);
+    else if (c.b_km && a.bn == 128)
+        e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<128, false, true>, tmA, tmB, tmC,
+                               tmAux, a);
     else if (c.b_km)
         e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<256, false, true>, tmA, tmB, tmC,
                                tmAux, a);

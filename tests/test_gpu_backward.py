@@ -75,6 +75,20 @@ def test_linear_backward_bf16(tp, cuda_device, kind):
     assert_bf16_parity(bf16_dev_to_f64(dW), rW, f"{kind} dW")
     assert_bf16_parity(dev_to_f64(dXf), rX, f"{kind} dX fp32", out_bf16=False)
     np.testing.assert_array_equal(dev_bits(dXf.to(torch.bfloat16)), dev_bits(dX))
+    # dX with 256- and 128-wide tiles: the same accumulation order per element
+    import os
+    outs = []
+    for plan in ("256", "128"):
+        os.environ["TP_GEMM_PLAN"] = plan
+        try:
+            dXp = torch.empty(M, K, dtype=torch.float32, device=cuda_device)
+            fn(X, W, dY, dXp, None, n_shards=n)
+        finally:
+            del os.environ["TP_GEMM_PLAN"]
+        outs.append(dev_bits(dXp))
+    assert tp.tp_get_device_status() == tp.TP_OK
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], dev_bits(dXf))
 
 
 @pytest.mark.parametrize("M,d,f,n", [(200, 256, 512, 2), (300, 264, 1000, 4),
