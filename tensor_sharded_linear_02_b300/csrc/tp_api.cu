@@ -598,51 +598,7 @@ tp_status column_impl(const void *X, const void *W, const void *bias, void *Y, v
     return launch_simt(X, W, Y, Ys, a, in_t, out_t, s);
 }
 
-}  // namespace
-
-// =================================================================== C ABI ==
-
-extern "C" {
-
-const char *tp_status_string(tp_status st) {
-    switch (st) {
-        case TP_OK: return "TP_OK";
-        case TP_ERR_NULL: return "TP_ERR_NULL: a required pointer is NULL";
-        case TP_ERR_SHAPE: return "TP_ERR_SHAPE: invalid or inconsistent sizes";
-        case TP_ERR_DIVISIBILITY: return "TP_ERR_DIVISIBILITY: split axis not divisible, or shard count out of range";
-        case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT: pointer or row pitch misaligned";
-        case TP_ERR_DTYPE: return "TP_ERR_DTYPE: unsupported dtype or activation";
-        case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace missing or too small";
-        case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA call failed";
-        case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
-        case TP_ERR_ALIAS: return "TP_ERR_ALIAS: an output overlaps an input";
-    }
-    return "TP_ERR_UNKNOWN";
-}
-
-tp_status tp_column_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
-                           int64_t K, int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
-                           tp_act act, cudaStream_t s) {
-    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
-}
-
-tp_status tp_column_linear_bias(const void *X, const void *W, const void *bias, void *Y,
-                                void *Y_shards, int64_t M, int64_t K, int64_t Nout, int n_shards,
-                                tp_dtype in_t, tp_dtype out_t, tp_act act, cudaStream_t s) {
-    return column_impl(X, W, bias, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
-}
-
-tp_status tp_column_linear_grouped(const void *X, const void *W, void *Y, void *Y_shards,
-                                   int64_t M, int64_t K, int64_t Nout, int n_shards,
-                                   int col_groups, tp_dtype in_t, tp_dtype out_t, tp_act act,
-                                   cudaStream_t s) {
-    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, col_groups, in_t, out_t,
-                       act, s);
-}
-
-}  // extern "C"
-
-namespace {
+// ------------------------------------------------------------ row split --
 
 tp_status row_impl(const void *X, const void *W, const void *bias, void *Y, float *P_out,
                    int64_t M, int64_t K, int64_t Nout, int n_shards, tp_dtype in_t,
@@ -719,9 +675,206 @@ tp_status row_impl(const void *X, const void *W, const void *bias, void *Y, floa
     return launch_simt(X, W, Y, nullptr, a, in_t, out_t, s);
 }
 
+// ------------------------------------------------------- segment copies --
+
+// Copies the segments of table t (all other fields filled by the caller)
+// from src [src_slots][rows][src_cols] to dst [dst_slots][rows][dst_cols].
+tp_status launch_segment_copy(const void *src, int64_t src_slots, int64_t src_cols, void *dst,
+                              int64_t dst_slots, int64_t dst_cols, int64_t rows, bool f32,
+                              SegTable &t, cudaStream_t s) {
+    DeviceInfo *dev = nullptr;
+    tp_status st = device_info(&dev);
+    if (st != TP_OK) return st;
+    const int64_t es = f32 ? 4 : 2;
+    t.box_rows = static_cast<int>(CAT_BOX_BYTES / (t.box_cols * es));
+    if (t.box_rows > 256) t.box_rows = 256;
+    t.units = (rows + t.box_rows - 1) / t.box_rows * t.col_boxes;
+    t.box_bytes = static_cast<uint32_t>(t.box_cols * t.box_rows * es);
+    t.wait_limit_ns = wait_limit_ns();
+    CUtensorMap tmSrc, tmDst;
+    if (!encode_3d_cached(&tmSrc, src, src_cols, rows, src_slots, src_cols * es,
+                          rows * src_cols * es, static_cast<uint32_t>(t.box_cols),
+                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_3d_cached(&tmDst, dst, dst_cols, rows, dst_slots, dst_cols * es,
+                          rows * dst_cols * es, static_cast<uint32_t>(t.box_cols),
+                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return TP_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    const int64_t grid = t.units < dev->sm_count ? t.units : dev->sm_count;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.dynamicSmemBytes = CAT_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, segment_copy_tma_kernel, tmSrc, tmDst, t) != cudaSuccess)
+        return TP_ERR_CUDA;
+    return launch_status();
+}
+
+// ------------------------------------------------------------ MLP block --
+
+tp_status mlp_impl(const void *X, const void *W1, const void *b1, const void *W2,
+                   const void *b2, void *Y, void *ws, size_t ws_bytes, int64_t M, int64_t d,
+                   int64_t f, int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
+    tp_status st = check_sizes(M, d, f);
+    if (st != TP_OK) return st;
+    if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    const size_t it = dtype_size(in_t), ot = dtype_size(out_t);
+    const size_t xb = M * d * it, w1b = d * f * it, w2b = f * d * it, yb = M * d * ot;
+    const size_t hb = M * f * it;
+    if (!present(X, xb) || !present(W1, w1b) || !present(W2, w2b) || !present(Y, yb))
+        return TP_ERR_NULL;
+    if ((st = check_shards(n_shards)) != TP_OK) return st;
+    if (f % n_shards != 0) return TP_ERR_DIVISIBILITY;
+    const size_t need = tp_mlp_block_workspace_size(M, f, in_t);
+    if (need > 0 && (!ws || ws_bytes < need)) return TP_ERR_WORKSPACE;
+    const size_t b1b = f * it, b2b = d * it;
+    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W1, w1b) || overlaps(Y, yb, W2, w2b) ||
+        overlaps(Y, yb, ws, hb) || overlaps(ws, hb, X, xb) || overlaps(ws, hb, W1, w1b) ||
+        overlaps(ws, hb, W2, w2b) || overlaps(Y, yb, b1, b1b) || overlaps(Y, yb, b2, b2b) ||
+        overlaps(ws, hb, b1, b1b) || overlaps(ws, hb, b2, b2b))
+        return TP_ERR_ALIAS;
+    if (in_t == TP_BF16) {
+        if (!aligned(X, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(Y, 16) ||
+            !aligned(ws, 16) || !aligned(b1, 16) || !aligned(b2, 16))
+            return TP_ERR_ALIGNMENT;
+        if (d % 8 != 0 || f % 8 != 0) return TP_ERR_ALIGNMENT;
+    } else {
+        if (!aligned(X, 4) || !aligned(W1, 4) || !aligned(W2, 4) || !aligned(Y, ot) ||
+            !aligned(ws, 4) || !aligned(b1, 4) || !aligned(b2, 4))
+            return TP_ERR_ALIGNMENT;
+    }
+    if (M == 0 || d == 0) return TP_OK;
+    if (f == 0)  // empty hidden layer: Y = b2 on every row (or 0)
+        return row_impl(nullptr, nullptr, b2, Y, nullptr, M, 0, d, 1, in_t, out_t, s);
+
+    if (in_t == TP_BF16) {
+        // step 1: H = GeLU(X . W1), column-parallel, H_i = column block i of H
+        GemmCall c1{};
+        c1.A = X; c1.B = W1; c1.M = M; c1.N = f; c1.K = d;
+        c1.k_groups = 1; c1.out = ws; c1.out_group_stride = 0; c1.out_f32 = false;
+        c1.gelu = true; c1.out_shards = nullptr; c1.n_shards = n_shards; c1.col_groups = 1;
+        c1.allow_split = true;
+        c1.bias = b1;  // each shard's slice of b1, before the GeLU
+        if ((st = launch_gemm(c1, s)) != TP_OK) return st;
+        // step 2: Y = sum_i H_i . W2_i, shard partials added in the accumulator
+        GemmCall c2{};
+        c2.A = ws; c2.B = W2; c2.M = M; c2.N = d; c2.K = f;
+        c2.k_groups = 1; c2.out = Y; c2.out_group_stride = 0; c2.out_f32 = (out_t == TP_F32);
+        c2.gelu = false; c2.out_shards = nullptr; c2.n_shards = n_shards; c2.col_groups = 1;
+        c2.allow_split = true;
+        c2.bias = b2;  // once, after the sum over all shards
+        return launch_gemm(c2, s);
+    }
+    SimtArgs a1{};
+    a1.M = M; a1.K = d; a1.N = f; a1.k_shards = 1; a1.act_gelu = 1; a1.partials = nullptr;
+    a1.bias = b1;
+    a1.shard_gw = f; a1.shard_sw = f; a1.shard_nl = f;
+    if ((st = launch_simt(X, W1, ws, nullptr, a1, TP_F32, TP_F32, s)) != TP_OK) return st;
+    SimtArgs a2{};
+    a2.M = M; a2.K = f; a2.N = d; a2.k_shards = n_shards; a2.act_gelu = 0; a2.partials = nullptr;
+    a2.bias = b2;
+    a2.shard_gw = d; a2.shard_sw = d; a2.shard_nl = d;
+    return launch_simt(ws, W2, Y, nullptr, a2, TP_F32, out_t, s);
+}
+
+// ------------------------------------------------------------- backward --
+
+// dW = X^T . dY  [K, N]  and  dX = dY . W^T  [M, K], bf16 inputs.  The two
+// products are the same for the column and the row split; only what a shard
+// owns differs (see include/tp.h).  Either output may be NULL.
+tp_status linear_backward_impl(const void *X, const void *W, const void *dY, void *dX, void *dW,
+                               int64_t M, int64_t K, int64_t N, tp_dtype in_t, tp_dtype out_t,
+                               cudaStream_t s) {
+    const size_t ot = dtype_size(out_t);
+    const size_t xb = M * K * 2, wb = K * N * 2, yb = M * N * 2;
+    const size_t dxb = M * K * ot, dwb = K * N * ot;
+    if (!present(X, xb) || !present(W, wb) || !present(dY, yb)) return TP_ERR_NULL;
+    if (in_t != TP_BF16 || !valid_dtype(out_t)) return TP_ERR_DTYPE;
+    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dY, 16) || !aligned(dX, 16) ||
+        !aligned(dW, 16) || K % 8 != 0 || N % 8 != 0)
+        return TP_ERR_ALIGNMENT;
+    const void *ins[3] = {X, W, dY};
+    const size_t inb[3] = {xb, wb, yb};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(dX, dxb, ins[i], inb[i]) || overlaps(dW, dwb, ins[i], inb[i]))
+            return TP_ERR_ALIAS;
+    if (overlaps(dX, dxb, dW, dwb)) return TP_ERR_ALIAS;
+    tp_status st;
+    if (dW && K > 0 && N > 0) {
+        if (M == 0) {
+            if (cudaMemsetAsync(dW, 0, dwb, s) != cudaSuccess) return TP_ERR_CUDA;
+        } else {
+            GemmCall c{};
+            c.A = X; c.a_mn = true;  // X^T: X is [M][K] = [K'][M'] with M' = K
+            c.B = dY;                // [M][N] = [K'][N']
+            c.M = K; c.N = N; c.K = M;
+            c.k_groups = 1; c.out = dW; c.out_f32 = (out_t == TP_F32);
+            c.n_shards = 1; c.col_groups = 1;
+            if ((st = launch_gemm(c, s)) != TP_OK) return st;
+        }
+    }
+    if (dX && M > 0 && K > 0) {
+        if (N == 0) {
+            if (cudaMemsetAsync(dX, 0, dxb, s) != cudaSuccess) return TP_ERR_CUDA;
+        } else {
+            GemmCall c{};
+            c.A = dY;                // [M][N]: K' = N walks the output columns (shards) in order
+            c.B = W; c.b_km = true;  // W^T: W is [K][N] = [N'][K'] with N' = K
+            c.M = M; c.N = K; c.K = N;
+            c.k_groups = 1; c.out = dX; c.out_f32 = (out_t == TP_F32);
+            c.n_shards = 1; c.col_groups = 1;
+            if ((st = launch_gemm(c, s)) != TP_OK) return st;
+        }
+    }
+    return TP_OK;
+}
+
 }  // namespace
 
+// =================================================================== C ABI ==
+
 extern "C" {
+
+const char *tp_status_string(tp_status st) {
+    switch (st) {
+        case TP_OK: return "TP_OK";
+        case TP_ERR_NULL: return "TP_ERR_NULL: a required pointer is NULL";
+        case TP_ERR_SHAPE: return "TP_ERR_SHAPE: invalid or inconsistent sizes";
+        case TP_ERR_DIVISIBILITY: return "TP_ERR_DIVISIBILITY: split axis not divisible, or shard count out of range";
+        case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT: pointer or row pitch misaligned";
+        case TP_ERR_DTYPE: return "TP_ERR_DTYPE: unsupported dtype or activation";
+        case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace missing or too small";
+        case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA call failed";
+        case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+        case TP_ERR_ALIAS: return "TP_ERR_ALIAS: an output overlaps an input";
+    }
+    return "TP_ERR_UNKNOWN";
+}
+
+tp_status tp_column_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
+                           int64_t K, int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
+                           tp_act act, cudaStream_t s) {
+    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
+}
+
+tp_status tp_column_linear_bias(const void *X, const void *W, const void *bias, void *Y,
+                                void *Y_shards, int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                tp_dtype in_t, tp_dtype out_t, tp_act act, cudaStream_t s) {
+    return column_impl(X, W, bias, Y, Y_shards, M, K, Nout, n_shards, 1, in_t, out_t, act, s);
+}
+
+tp_status tp_column_linear_grouped(const void *X, const void *W, void *Y, void *Y_shards,
+                                   int64_t M, int64_t K, int64_t Nout, int n_shards,
+                                   int col_groups, tp_dtype in_t, tp_dtype out_t, tp_act act,
+                                   cudaStream_t s) {
+    return column_impl(X, W, nullptr, Y, Y_shards, M, K, Nout, n_shards, col_groups, in_t, out_t,
+                       act, s);
+}
 
 tp_status tp_row_linear(const void *X, const void *W, void *Y, float *P_out, int64_t M, int64_t K,
                         int64_t Nout, int n_shards, tp_dtype in_t, tp_dtype out_t,
@@ -824,52 +977,6 @@ tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t
     return launch_status();
 }
 
-}  // extern "C"
-
-namespace {
-
-// Copies the segments of table t (all other fields filled by the caller)
-// from src [src_slots][rows][src_cols] to dst [dst_slots][rows][dst_cols].
-tp_status launch_segment_copy(const void *src, int64_t src_slots, int64_t src_cols, void *dst,
-                              int64_t dst_slots, int64_t dst_cols, int64_t rows, bool f32,
-                              SegTable &t, cudaStream_t s) {
-    DeviceInfo *dev = nullptr;
-    tp_status st = device_info(&dev);
-    if (st != TP_OK) return st;
-    const int64_t es = f32 ? 4 : 2;
-    t.box_rows = static_cast<int>(CAT_BOX_BYTES / (t.box_cols * es));
-    if (t.box_rows > 256) t.box_rows = 256;
-    t.units = (rows + t.box_rows - 1) / t.box_rows * t.col_boxes;
-    t.box_bytes = static_cast<uint32_t>(t.box_cols * t.box_rows * es);
-    t.wait_limit_ns = wait_limit_ns();
-    CUtensorMap tmSrc, tmDst;
-    if (!encode_3d_cached(&tmSrc, src, src_cols, rows, src_slots, src_cols * es,
-                          rows * src_cols * es, static_cast<uint32_t>(t.box_cols),
-                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_3d_cached(&tmDst, dst, dst_cols, rows, dst_slots, dst_cols * es,
-                          rows * dst_cols * es, static_cast<uint32_t>(t.box_cols),
-                          static_cast<uint32_t>(t.box_rows), 1, f32, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return TP_ERR_CUDA;
-    cudaLaunchConfig_t cfg{};
-    const int64_t grid = t.units < dev->sm_count ? t.units : dev->sm_count;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(32, 1, 1);
-    cfg.dynamicSmemBytes = CAT_SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, segment_copy_tma_kernel, tmSrc, tmDst, t) != cudaSuccess)
-        return TP_ERR_CUDA;
-    return launch_status();
-}
-
-}  // namespace
-
-extern "C" {
-
 tp_status tp_qkv_linear(const void *X, const void *W, void *Y, void *Y_shards, int64_t M,
                         int64_t K, int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim,
                         int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
@@ -939,79 +1046,6 @@ size_t tp_mlp_block_workspace_size(int64_t M, int64_t f, tp_dtype t) {
     return (b + 255) & ~static_cast<size_t>(255);
 }
 
-}  // extern "C"
-
-namespace {
-
-tp_status mlp_impl(const void *X, const void *W1, const void *b1, const void *W2,
-                   const void *b2, void *Y, void *ws, size_t ws_bytes, int64_t M, int64_t d,
-                   int64_t f, int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
-    tp_status st = check_sizes(M, d, f);
-    if (st != TP_OK) return st;
-    if (!valid_dtype(in_t) || !valid_dtype(out_t)) return TP_ERR_DTYPE;
-    const size_t it = dtype_size(in_t), ot = dtype_size(out_t);
-    const size_t xb = M * d * it, w1b = d * f * it, w2b = f * d * it, yb = M * d * ot;
-    const size_t hb = M * f * it;
-    if (!present(X, xb) || !present(W1, w1b) || !present(W2, w2b) || !present(Y, yb))
-        return TP_ERR_NULL;
-    if ((st = check_shards(n_shards)) != TP_OK) return st;
-    if (f % n_shards != 0) return TP_ERR_DIVISIBILITY;
-    const size_t need = tp_mlp_block_workspace_size(M, f, in_t);
-    if (need > 0 && (!ws || ws_bytes < need)) return TP_ERR_WORKSPACE;
-    const size_t b1b = f * it, b2b = d * it;
-    if (overlaps(Y, yb, X, xb) || overlaps(Y, yb, W1, w1b) || overlaps(Y, yb, W2, w2b) ||
-        overlaps(Y, yb, ws, hb) || overlaps(ws, hb, X, xb) || overlaps(ws, hb, W1, w1b) ||
-        overlaps(ws, hb, W2, w2b) || overlaps(Y, yb, b1, b1b) || overlaps(Y, yb, b2, b2b) ||
-        overlaps(ws, hb, b1, b1b) || overlaps(ws, hb, b2, b2b))
-        return TP_ERR_ALIAS;
-    if (in_t == TP_BF16) {
-        if (!aligned(X, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(Y, 16) ||
-            !aligned(ws, 16) || !aligned(b1, 16) || !aligned(b2, 16))
-            return TP_ERR_ALIGNMENT;
-        if (d % 8 != 0 || f % 8 != 0) return TP_ERR_ALIGNMENT;
-    } else {
-        if (!aligned(X, 4) || !aligned(W1, 4) || !aligned(W2, 4) || !aligned(Y, ot) ||
-            !aligned(ws, 4) || !aligned(b1, 4) || !aligned(b2, 4))
-            return TP_ERR_ALIGNMENT;
-    }
-    if (M == 0 || d == 0) return TP_OK;
-    if (f == 0)  // empty hidden layer: Y = b2 on every row (or 0)
-        return row_impl(nullptr, nullptr, b2, Y, nullptr, M, 0, d, 1, in_t, out_t, s);
-
-    if (in_t == TP_BF16) {
-        // step 1: H = GeLU(X . W1), column-parallel, H_i = column block i of H
-        GemmCall c1{};
-        c1.A = X; c1.B = W1; c1.M = M; c1.N = f; c1.K = d;
-        c1.k_groups = 1; c1.out = ws; c1.out_group_stride = 0; c1.out_f32 = false;
-        c1.gelu = true; c1.out_shards = nullptr; c1.n_shards = n_shards; c1.col_groups = 1;
-        c1.allow_split = true;
-        c1.bias = b1;  // each shard's slice of b1, before the GeLU
-        if ((st = launch_gemm(c1, s)) != TP_OK) return st;
-        // step 2: Y = sum_i H_i . W2_i, shard partials added in the accumulator
-        GemmCall c2{};
-        c2.A = ws; c2.B = W2; c2.M = M; c2.N = d; c2.K = f;
-        c2.k_groups = 1; c2.out = Y; c2.out_group_stride = 0; c2.out_f32 = (out_t == TP_F32);
-        c2.gelu = false; c2.out_shards = nullptr; c2.n_shards = n_shards; c2.col_groups = 1;
-        c2.allow_split = true;
-        c2.bias = b2;  // once, after the sum over all shards
-        return launch_gemm(c2, s);
-    }
-    SimtArgs a1{};
-    a1.M = M; a1.K = d; a1.N = f; a1.k_shards = 1; a1.act_gelu = 1; a1.partials = nullptr;
-    a1.bias = b1;
-    a1.shard_gw = f; a1.shard_sw = f; a1.shard_nl = f;
-    if ((st = launch_simt(X, W1, ws, nullptr, a1, TP_F32, TP_F32, s)) != TP_OK) return st;
-    SimtArgs a2{};
-    a2.M = M; a2.K = f; a2.N = d; a2.k_shards = n_shards; a2.act_gelu = 0; a2.partials = nullptr;
-    a2.bias = b2;
-    a2.shard_gw = d; a2.shard_sw = d; a2.shard_nl = d;
-    return launch_simt(ws, W2, Y, nullptr, a2, TP_F32, out_t, s);
-}
-
-}  // namespace
-
-extern "C" {
-
 tp_status tp_mlp_block(const void *X, const void *W1, const void *W2, void *Y, void *ws,
                        size_t ws_bytes, int64_t M, int64_t d, int64_t f, int n_shards,
                        tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
@@ -1027,60 +1061,6 @@ tp_status tp_mlp_block_bias(const void *X, const void *W1, const void *b1, const
 }
 
 // ----------------------------------------------------------- backward ----
-
-namespace {
-
-// dW = X^T . dY  [K, N]  and  dX = dY . W^T  [M, K], bf16 inputs.  The two
-// products are the same for the column and the row split; only what a shard
-// owns differs (see include/tp.h).  Either output may be NULL.
-tp_status linear_backward_impl(const void *X, const void *W, const void *dY, void *dX, void *dW,
-                               int64_t M, int64_t K, int64_t N, tp_dtype in_t, tp_dtype out_t,
-                               cudaStream_t s) {
-    const size_t ot = dtype_size(out_t);
-    const size_t xb = M * K * 2, wb = K * N * 2, yb = M * N * 2;
-    const size_t dxb = M * K * ot, dwb = K * N * ot;
-    if (!present(X, xb) || !present(W, wb) || !present(dY, yb)) return TP_ERR_NULL;
-    if (in_t != TP_BF16 || !valid_dtype(out_t)) return TP_ERR_DTYPE;
-    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dY, 16) || !aligned(dX, 16) ||
-        !aligned(dW, 16) || K % 8 != 0 || N % 8 != 0)
-        return TP_ERR_ALIGNMENT;
-    const void *ins[3] = {X, W, dY};
-    const size_t inb[3] = {xb, wb, yb};
-    for (int i = 0; i < 3; ++i)
-        if (overlaps(dX, dxb, ins[i], inb[i]) || overlaps(dW, dwb, ins[i], inb[i]))
-            return TP_ERR_ALIAS;
-    if (overlaps(dX, dxb, dW, dwb)) return TP_ERR_ALIAS;
-    tp_status st;
-    if (dW && K > 0 && N > 0) {
-        if (M == 0) {
-            if (cudaMemsetAsync(dW, 0, dwb, s) != cudaSuccess) return TP_ERR_CUDA;
-        } else {
-            GemmCall c{};
-            c.A = X; c.a_mn = true;  // X^T: X is [M][K] = [K'][M'] with M' = K
-            c.B = dY;                // [M][N] = [K'][N']
-            c.M = K; c.N = N; c.K = M;
-            c.k_groups = 1; c.out = dW; c.out_f32 = (out_t == TP_F32);
-            c.n_shards = 1; c.col_groups = 1;
-            if ((st = launch_gemm(c, s)) != TP_OK) return st;
-        }
-    }
-    if (dX && M > 0 && K > 0) {
-        if (N == 0) {
-            if (cudaMemsetAsync(dX, 0, dxb, s) != cudaSuccess) return TP_ERR_CUDA;
-        } else {
-            GemmCall c{};
-            c.A = dY;                // [M][N]: K' = N walks the output columns (shards) in order
-            c.B = W; c.b_km = true;  // W^T: W is [K][N] = [N'][K'] with N' = K
-            c.M = M; c.N = K; c.K = N;
-            c.k_groups = 1; c.out = dX; c.out_f32 = (out_t == TP_F32);
-            c.n_shards = 1; c.col_groups = 1;
-            if ((st = launch_gemm(c, s)) != TP_OK) return st;
-        }
-    }
-    return TP_OK;
-}
-
-}  // namespace
 
 tp_status tp_column_linear_backward(const void *X, const void *W, const void *dY, void *dX,
                                     void *dW, int64_t M, int64_t K, int64_t Nout, int n_shards,
