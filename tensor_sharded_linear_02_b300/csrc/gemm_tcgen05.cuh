@@ -42,17 +42,12 @@
 //       shard 1's, ..., so the row-parallel partial sums are added inside the
 //       accumulator.
 //   gemm_cluster_sum_kernel  256-wide tiles for outputs with too few tiles to
-//       fill the GPU: the S pairs of a cluster share one output tile, pair p
-//       accumulates the p-th contiguous slice of the K blocks (with K/n a
-//       multiple of the block depth and S dividing n, slice p is exactly
-//       shard group p).  The S CTAs holding the same 128 rows (one per pair)
-//       split them: CTA of pair p owns rows [p*128/S, (p+1)*128/S) of that
-//       half.  Once every main loop of the cluster is done (a cluster
-//       barrier: from then on no ring is in use), every CTA stores the fp32
-//       partial rows it holds into slot `its pair` of the owner's shared
-//       memory (distributed shared memory stores), and after a second
-//       barrier each owner adds its S slots in ascending slice order.  The
-//       sum never touches HBM.
+//       fill the GPU: the two pairs of a cluster of 4 share one output tile,
+//       pair p accumulating the p-th half of the K blocks (with K/n a
+//       multiple of 256 and n even, half p is exactly shard group p).  Each
+//       CTA sends the 64 accumulator rows its partner owns, in 4 KiB bulk
+//       copies between shared memories, and adds the partner's chunks to
+//       its own rows as they land; the sum never touches HBM.
 #pragma once
 
 #include "tp_device.cuh"
@@ -88,13 +83,10 @@ struct Ring {
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int SMEM_BYTES = RING_BYTES + EPI_WARPS * STG_BYTES + 1024 + 256;
+    static constexpr int SMEM_BYTES = RING_BYTES + EPI_WARPS * STG_BYTES + 1024 + 512;
     static_assert(STAGES <= MAX_STAGES, "barrier array");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
-
-constexpr int RED_LD = MAX_BN + 4;  // fp32 row pitch of the parked partial tile (bank spread)
-static_assert(BM * RED_LD * 4 <= Ring<256>::RING_BYTES, "partial tile must fit in the ring");
 
 // A descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart;
 // a stage holds two such boxes (K 0..63 and 64..127), 16 KiB apart.
@@ -110,10 +102,12 @@ struct SmemBarriers {
     uint64_t acc_full[2];        // both CTAs: accumulator ready (multicast commit)
     uint64_t acc_empty[2];       // even CTA: epilogue warps of both CTAs done
     uint64_t drain;
+    uint64_t ready;              // split kernel: the partner's ring is free
+    uint64_t xfer[16];           // split kernel: one partial-row chunk landed
     uint32_t tmem_base;
     uint32_t abort;
 };
-static_assert(sizeof(SmemBarriers) <= 256, "barrier block");
+static_assert(sizeof(SmemBarriers) <= 512, "barrier block");
 
 // Epilogue modes of the TMA-store path (bf16 outputs):
 //   EPI_PLAIN      out = act(acc)                      -> tmC
@@ -172,7 +166,7 @@ __device__ __forceinline__ void store_vec8(const GemmArgs &a, int g, int row, in
     if (a.bias) add_bias8(a.bias, col, f);
     if (a.act_gelu) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = gelu_f32(f[i]);
+        for (int i = 0; i < 8; i += 2) gelu2_f32(f[i], f[i + 1]);
     }
     uint4 u;
     if (!a.out_f32)
@@ -311,22 +305,15 @@ __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool 
                 bias_chunk32(bias, N, col_base + cofs + c, r0);
                 bias_chunk32(bias, N, col_base + cofs + c + 32, r1);
             }
-            uint32_t pk[32];
             if (gelu) {
+                gelu_chunk32(r0);
+                gelu_chunk32(r1);
+            }
+            uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    pk[i] = pack_bf16x2(gelu_f32(__uint_as_float(r0[2 * i])),
-                                        gelu_f32(__uint_as_float(r0[2 * i + 1])));
-                    pk[16 + i] = pack_bf16x2(gelu_f32(__uint_as_float(r1[2 * i])),
-                                             gelu_f32(__uint_as_float(r1[2 * i + 1])));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-                    pk[16 + i] =
-                        pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-                }
+            for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                pk[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
             }
             stage_and_store_box(tmC, stg, pk, col_base + cofs + c, row0, g);
         }
@@ -338,10 +325,7 @@ __device__ __forceinline__ void epilogue_tma_store(const CUtensorMap *tmC, bool 
             tmem_ld_wait();
             if (c + 32 >= ncols) release_accumulator(acc_empty_addr);
             if (bias) bias_chunk32(bias, N, col_base + cofs + c, r);
-            if (gelu) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gelu_f32(__uint_as_float(r[i])));
-            }
+            if (gelu) gelu_chunk32(r);
             stage_and_store_box(tmC, stg, r, col_base + cofs + c, row0, g);
         }
     }
@@ -366,12 +350,12 @@ __device__ __forceinline__ void epilogue_dual(const CUtensorMap *tmC, const CUte
             pk[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
         }
         stage_and_store_box(tmC, stg, pk, col_base + cofs + c, row0, 0);
+        gelu_chunk32(r0);
+        gelu_chunk32(r1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            pk[i] = pack_bf16x2(gelu_f32(__uint_as_float(r0[2 * i])),
-                                gelu_f32(__uint_as_float(r0[2 * i + 1])));
-            pk[16 + i] = pack_bf16x2(gelu_f32(__uint_as_float(r1[2 * i])),
-                                     gelu_f32(__uint_as_float(r1[2 * i + 1])));
+            pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            pk[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
         }
         stage_and_store_box(tmAux, stg, pk, col_base + cofs + c, row0, 0);
     }
@@ -587,7 +571,8 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // next kernel of the stream may start launching, and this one waits for the
 // previous kernel to complete.
 __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, int stages, uint32_t tmem_cols,
-                                           const CUtensorMap *const *maps, int nmaps) {
+                                           const CUtensorMap *const *maps, int nmaps,
+                                           bool split_barriers = false) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -599,6 +584,10 @@ __device__ __forceinline__ void gemm_setup(SmemBarriers *bars, int stages, uint3
             mbar_init(smem_u32(&bars->acc_empty[i]), 2 * EPI_WARPS);
         }
         mbar_init(smem_u32(&bars->drain), 1);
+        if (split_barriers) {
+            mbar_init(smem_u32(&bars->ready), 1);
+            for (int i = 0; i < 16; ++i) mbar_init(smem_u32(&bars->xfer[i]), 1);
+        }
         bars->abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -727,7 +716,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 epilogue_direct(a, taddr, row0 + lane, nt * bn, cofs, bn / 2, g, release);
             }
         }
-        if (lane == 0) bulk_wait0();  // every store box has left shared memory and landed
+        if (lane == 0) bulk_wait_read0();  // every store box has left shared memory
         __syncwarp();
     }
 
@@ -735,9 +724,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Cluster split kernel (256-wide tiles): grid = 2 * S * tiles CTAs, cluster =
-// 2 * S CTAs along x (S pairs; cluster rank 2p + h is half h of pair p).
+// Cluster split kernel (256-wide tiles, two pairs per tile): grid = 4 * tiles
+// CTAs, cluster = 4 CTAs along x (cluster rank 2p + h is half h of pair p).
+// Pair p accumulates K slice p.  The two CTAs that hold the same 128 rows
+// (ranks h and 2 + h, partners) split them: pair p owns rows [64p, 64p + 64)
+// of the half.  Each epilogue warp covers 32 rows (its tensor-memory lane
+// quadrant) and 128 columns; a warp whose rows the partner owns is a sender,
+// the partner's warp with the same rows and columns its receiver (one of
+// four links).  The sender moves its 32 x 128 fp32 partial in four chunks of
+// 32 columns: tensor memory -> its own shared memory (16-byte chunk v of row
+// r at v ^ (r mod 8): conflict-free) -> one bulk copy into the receiver's
+// shared memory, counted on the receiver's barrier for that chunk.  The
+// receiver adds each chunk to its own partial as it lands (two fp32
+// operands: the sum does not depend on their order) and stores the result,
+// so the transfer overlaps the epilogue.  Chunks land in the receiver's
+// operand ring, so a sender first waits until the partner's main loop is
+// done (`ready`, arrived on by the partner).  The sum never touches HBM.
 // ---------------------------------------------------------------------------
+constexpr int XFER_COLS = 32;                            // columns per chunk
+constexpr int XFER_BYTES = 32 * XFER_COLS * 4;           // 32 rows x 32 fp32
+constexpr int XFER_CHUNKS = (MAX_BN / 2) / XFER_COLS;    // chunks per link
+constexpr int XFER_LINKS = 4;                            // (row block, column half)
+static_assert(XFER_LINKS * XFER_CHUNKS <= 16, "transfer barriers");
+static_assert(2 * XFER_LINKS * XFER_CHUNKS * XFER_BYTES <= Ring<256>::RING_BYTES,
+              "send and receive areas fit in the ring");
+
+__device__ __forceinline__ uint32_t xfer_slot(uint32_t buf, int lane, int v) {
+    return buf + lane * (XFER_COLS * 4) + ((v ^ (lane & 7)) << 4);
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_cluster_sum_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -752,26 +767,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     constexpr uint32_t TMEM_COLS = BN;
 
-    const int S = a.split;
     const int rank = static_cast<int>(cluster_ctarank());
     const int p = rank >> 1;      // pair = K slice
     const int half = rank & 1;    // which 128 rows of the tile
     const bool leader = half == 0;
-    const int tile = blockIdx.x / (2 * S);
+    const uint32_t partner = static_cast<uint32_t>(rank ^ 2);
+    const int tile = blockIdx.x / 4;
     const int mt = tile % a.m_tiles;
     const int nt = tile / a.m_tiles;
-    const int kb0 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * p) / S);
-    const int kb1 = static_cast<int>((static_cast<int64_t>(a.k_blocks) * (p + 1)) / S);
+    const int kb0 = p == 0 ? 0 : a.k_blocks / 2;
+    const int kb1 = p == 0 ? a.k_blocks / 2 : a.k_blocks;
 
-    const CUtensorMap *maps[2] = {&tmA, &tmB};
-    gemm_setup(bars, R::STAGES, TMEM_COLS, maps, 2);
+    const CUtensorMap *maps[3] = {&tmA, &tmB, &tmC};
+    gemm_setup(bars, R::STAGES, TMEM_COLS, maps, a.tma_store ? 3 : 2, true);
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
-    float *red = reinterpret_cast<float *>(ring);  // parks the fp32 partial tile
     const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * p));
 
     if (warp == 0) {
         if (lane == 0) {
+            // every chunk this CTA receives: 4 KiB each
+            for (int i = 0; i < XFER_LINKS * XFER_CHUNKS; ++i)
+                mbar_arrive_expect_tx(smem_u32(&bars->xfer[i]), XFER_BYTES);
             const uint32_t full_remote =
                 dsmem_map(smem_u32(&bars->full[0]), static_cast<uint32_t>(2 * p));
             ProducerState ps;
@@ -794,78 +811,115 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        if (mbar_wait_warp(smem_u32(&bars->acc_full[0]), 0, limit, &bars->abort,
-                           SITE_EPI_ACC_FULL))
-            tc_fence_after();
-    }
-
-    // Every CTA of the cluster has finished its main loop: from here on no
-    // ring is in use by TMA or MMA, so each can take parked partial rows.
-    cluster_sync_all();
-
-    if (warp >= 2 && !bars->abort) {
-        // Push: row `rit` of this CTA's fp32 partial (row half*128 + rit of
-        // the tile) goes to slot `p` of its owner's parking area
-        // [S][BM/S][RED_LD]; the owner is the CTA of the same half in pair
-        // rit / (BM/S).
-        fence_proxy_async_smem();
-        const int q = warp & 3;
-        const int cofs = ((warp - 2) >> 2) * (BN / 2);
-        const int rows_per = BM / S;
-        const int rit = q * 32 + lane;
-        const int owner_p = rit / rows_per;
-        const int owner = 2 * owner_p + half;
-        const int slot_row = p * rows_per + (rit - owner_p * rows_per);
-        float *dst = red + slot_row * RED_LD;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        // The transfer runs whether or not a wait gave up before (then the
+        // rows are meaningless), so that every chunk lands before the CTAs
+        // exit.
+        const bool acc_ok = mbar_wait_warp(smem_u32(&bars->acc_full[0]), 0, limit, &bars->abort,
+                                           SITE_EPI_ACC_FULL);
+        if (acc_ok) tc_fence_after();
+        // This CTA's main loop is done, its ring free: the partner may send.
+        if (warp == 2 && lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&bars->ready), partner));
+        const int q = warp & 3;              // tensor-memory lane quadrant
+        const int chalf = (warp - 2) >> 2;   // column half
+        const int cofs = chalf * (BN / 2);
+        const int link = (q & 1) + 2 * chalf;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cofs;
+        const uint32_t send = smem_u32(ring) + link * XFER_CHUNKS * XFER_BYTES;
+        const uint32_t recv = send + XFER_LINKS * XFER_CHUNKS * XFER_BYTES;
+        if ((q >> 1) != p) {
+            // sender: the partner owns these rows
 #pragma unroll 1
-        for (int c = cofs; c < cofs + BN / 2; c += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + c, r);
-            tmem_ld_wait();
+            for (int c = 0; c < XFER_CHUNKS; ++c) {
+                const uint32_t buf = send + c * XFER_BYTES;
+                if (acc_ok) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + c * XFER_COLS, r);
+                    tmem_ld_wait();
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 val =
-                    make_float4(__uint_as_float(r[v * 4 + 0]), __uint_as_float(r[v * 4 + 1]),
-                                __uint_as_float(r[v * 4 + 2]), __uint_as_float(r[v * 4 + 3]));
-                float *ptr = dst + c + v * 4;
-                if (owner == rank)
-                    *reinterpret_cast<float4 *>(ptr) = val;
-                else
-                    dsmem_st_f4(dsmem_map(smem_u32(ptr), static_cast<uint32_t>(owner)), val);
+                    for (int v = 0; v < 8; ++v)
+                        st_shared_v4(xfer_slot(buf, lane, v), r[4 * v], r[4 * v + 1],
+                                     r[4 * v + 2], r[4 * v + 3]);
+                }
+                fence_proxy_async_smem();  // generic-proxy writes -> the bulk copy
+                __syncwarp();
+                if (lane == 0) {
+                    if (c == 0) mbar_wait_drain(smem_u32(&bars->ready), 0, limit);
+                    bulk_copy_to_peer(
+                        dsmem_map(recv + c * XFER_BYTES, partner), buf, XFER_BYTES,
+                        dsmem_map(smem_u32(&bars->xfer[link * XFER_CHUNKS + c]), partner));
+                }
             }
+        } else if (acc_ok) {
+            // receiver: own rows, 64 columns (two chunks) at a time
+            const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
+            const int row0 = mt * PAIR_M + half * BM + q * 32;
+            const int col0 = nt * BN + cofs;
+#pragma unroll 1
+            for (int c = 0; c < XFER_CHUNKS; c += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(taddr + c * XFER_COLS, r0);
+                tmem_ld_32x32b_x32(taddr + (c + 1) * XFER_COLS, r1);
+                const bool ok0 = mbar_wait_warp(smem_u32(&bars->xfer[link * XFER_CHUNKS + c]), 0,
+                                                limit, &bars->abort, SITE_EPI_SPLIT);
+                const bool ok1 =
+                    ok0 && mbar_wait_warp(smem_u32(&bars->xfer[link * XFER_CHUNKS + c + 1]), 0,
+                                          limit, &bars->abort, SITE_EPI_SPLIT);
+                tmem_ld_wait();
+                if (!ok1) break;
+                const uint32_t b0 = recv + c * XFER_BYTES, b1 = b0 + XFER_BYTES;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 u0 = ld_shared_v4(xfer_slot(b0, lane, v));
+                    const uint4 u1 = ld_shared_v4(xfer_slot(b1, lane, v));
+                    const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
+                    const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        r0[4 * v + i] = __float_as_uint(__uint_as_float(r0[4 * v + i]) +
+                                                        __uint_as_float(w0[i]));
+                        r1[4 * v + i] = __float_as_uint(__uint_as_float(r1[4 * v + i]) +
+                                                        __uint_as_float(w1[i]));
+                    }
+                }
+                const int col = col0 + c * XFER_COLS;
+                if (!a.tma_store) {  // shard-major copy requested: direct stores
+                    store_row_chunk32(a, 0, row0 + lane, col, r0);
+                    store_row_chunk32(a, 0, row0 + lane, col + XFER_COLS, r1);
+                    continue;
+                }
+                if (a.bias) {
+                    bias_chunk32(a.bias, a.N, col, r0);
+                    bias_chunk32(a.bias, a.N, col + XFER_COLS, r1);
+                }
+                if (a.act_gelu) {
+                    gelu_chunk32(r0);
+                    gelu_chunk32(r1);
+                }
+                if (a.out_f32) {  // boxes of 32 fp32 columns
+                    stage_and_store_box(&tmC, stg, r0, col, row0, 0);
+                    stage_and_store_box(&tmC, stg, r1, col + XFER_COLS, row0, 0);
+                } else {  // boxes of 64 bf16 columns
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]),
+                                            __uint_as_float(r0[2 * i + 1]));
+                        pk[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
+                                                 __uint_as_float(r1[2 * i + 1]));
+                    }
+                    stage_and_store_box(&tmC, stg, pk, col, row0, 0);
+                }
+            }
+            if (lane == 0) bulk_wait_read0();  // every store box has left shared memory
+            __syncwarp();
         }
     }
-
-    // Every CTA of the cluster has delivered its partial rows.
-    cluster_sync_all();
-
-    if (warp >= 2 && !bars->abort) {
-        // Owner: rows [p*BM/S, (p+1)*BM/S) of half `half` of the tile, S
-        // slots each, added in ascending slice order from local shared memory.
-        const int rows_per = BM / S;
-        const int cl = lane * 8;  // 8 consecutive columns per lane, BN = 32 * 8
-        for (int rr = warp - 2; rr < rows_per; rr += EPI_WARPS) {
-            const int row = mt * PAIR_M + half * BM + p * rows_per + rr;
-            const float *src = red + rr * RED_LD + cl;
-            float4 s0 = *reinterpret_cast<const float4 *>(src);
-            float4 s1 = *reinterpret_cast<const float4 *>(src + 4);
-            for (int j = 1; j < S; ++j) {
-                const float *sp = src + j * rows_per * RED_LD;
-                const float4 t0 = *reinterpret_cast<const float4 *>(sp);
-                const float4 t1 = *reinterpret_cast<const float4 *>(sp + 4);
-                s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
-                s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
-            }
-            const int col = nt * BN + cl;
-            if (row < a.M && col < a.N) {
-                float f[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                store_vec8(a, 0, row, col, f);
-            }
-        }
+    // Every chunk the partner sends has landed before this CTA may exit.
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < XFER_LINKS * XFER_CHUNKS; ++i)
+            mbar_wait_drain(smem_u32(&bars->xfer[i]), 0, limit);
     }
-
-    gemm_teardown(tmem_base, TMEM_COLS);
+    gemm_teardown(tmem_base, TMEM_COLS);  // cluster barrier: no copy reads a CTA that left
 }
 
 }  // namespace tpk

@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(32, 1)
     for (int64_t j = stored; j < issued; ++j)
         mbar_wait_drain(smem_u32(&full[j % CAT_STAGES]),
                         static_cast<uint32_t>((j / CAT_STAGES) & 1), a.wait_limit_ns);
-    bulk_wait0();
+    bulk_wait_read0();  // the stores have left shared memory
 }
 
 // Column-segment copy with TMA boxes: the same ring as the concat, driven
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(32, 1)
     for (int64_t j = stored; j < issued; ++j)
         mbar_wait_drain(smem_u32(&full[j % CAT_STAGES]),
                         static_cast<uint32_t>((j / CAT_STAGES) & 1), t.wait_limit_ns);
-    bulk_wait0();
+    bulk_wait_read0();  // the stores have left shared memory
 }
 
 }  // namespace tpk

@@ -26,7 +26,7 @@ constexpr int64_t kInt32Max = 0x7FFFFFFF;
 struct DeviceInfo {
     int sm_count = 0;
     int max_pairs = 0;          // clusters of 2 GEMM CTAs that fit at once
-    int max_clusters[5] = {};   // index log2(S): clusters of 2*S GEMM CTAs that fit at once
+    int max_split_clusters = 0;  // clusters of 4 CTAs (two pairs) of the split kernel at once
     bool ready = false;
 };
 
@@ -106,10 +106,8 @@ tp_status device_info(DeviceInfo **out) {
             reinterpret_cast<const void *>(gemm_persistent_kernel<128>), 2, Ring<128>::SMEM_BYTES);
         if (p128 < d.max_pairs) d.max_pairs = p128;
         if (d.max_pairs < 1) return TP_ERR_CUDA;
-        for (int l = 1; l <= 2; ++l)  // S = 2, 4 pairs: clusters of 4 and 8 CTAs
-            d.max_clusters[l] = active_clusters(
-                reinterpret_cast<const void *>(gemm_cluster_sum_kernel), 2 << l,
-                Ring<256>::SMEM_BYTES);
+        d.max_split_clusters = active_clusters(
+            reinterpret_cast<const void *>(gemm_cluster_sum_kernel), 4, Ring<256>::SMEM_BYTES);
         d.ready = true;
     }
     *out = &d;
@@ -263,15 +261,15 @@ struct GemmCall {
     const void *bias = nullptr;  // bf16 [N], added before the activation
 };
 
-// Launch plan of one GEMM: tile width and, for the cluster split kernel,
-// pairs per cluster S (S = 1: persistent kernel).
+// Launch plan of one GEMM: tile width, and split = 2 for the cluster split
+// kernel (two pairs per tile), 1 for the persistent kernel.
 struct GemmPlan {
     int bn = 256;
     int split = 1;
 };
 
 // Optional override of the automatic plan, for measurements:
-// TP_GEMM_PLAN = "256" | "128" | "split2" | "split4".
+// TP_GEMM_PLAN = "256" | "128" | "split2".
 // Read at every launch, so that a process can compare plans.
 int plan_override() {
     const char *e = std::getenv("TP_GEMM_PLAN");
@@ -279,7 +277,6 @@ int plan_override() {
     if (!std::strcmp(e, "256")) return 1;
     if (!std::strcmp(e, "128")) return 2;
     if (!std::strcmp(e, "split2")) return 3;
-    if (!std::strcmp(e, "split4")) return 4;
     return 0;
 }
 
@@ -287,8 +284,9 @@ int plan_override() {
 // of a 256-wide pair tile (128 deep, about 1024 tensor-core cycles):
 //   persistent, width bn: waves * k_blocks * (bn / 256) * overhead(bn) plus
 //       the exposed epilogue of the last tile (larger with GeLU);
-//   split over S pairs (256-wide, one wave of clusters): k_blocks / S plus
-//       the shared-memory reduction of the partial tiles.
+//   split over two pairs (256-wide, one wave of clusters): k_blocks / 2
+//       plus the exchange of the partial rows between the two pairs (64 KiB
+//       of fp32 per CTA through distributed shared memory) and the tail.
 // A 128-wide k-block carries half the tensor work of a 256-wide one but the
 // same issue work (MMA and TMA instructions per stage) and 3/4 of its
 // operand bytes; measured, it takes about 0.75 of the 256-wide time.
@@ -308,21 +306,19 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int k_blocks, int k_groups, bool allow_
         cbest = c128;
     }
     const bool can_split = allow_split && k_groups == 1;
-    for (int l = 1; l <= 2 && can_split; ++l) {
-        const int S = 1 << l;
-        if (u256 > dev.max_clusters[l] || S > k_blocks) continue;
-        const double cs = static_cast<double>(k_blocks) / S + 12.0 + tail;
+    const bool split_fits = can_split && u256 <= dev.max_split_clusters && k_blocks >= 2;
+    if (split_fits) {
+        const double cs = static_cast<double>((k_blocks + 1) / 2) + 4.0 + tail;
         if (cs < cbest) {
             best.bn = 256;
-            best.split = S;
+            best.split = 2;
             cbest = cs;
         }
     }
     switch (plan_override()) {
         case 1: return GemmPlan{256, 1};
         case 2: return GemmPlan{128, 1};
-        case 3: if (can_split && u256 <= dev.max_clusters[1] && k_blocks >= 2) return GemmPlan{256, 2}; break;
-        case 4: if (can_split && u256 <= dev.max_clusters[2] && k_blocks >= 4) return GemmPlan{256, 4}; break;
+        case 3: if (split_fits) return GemmPlan{256, 2}; break;
         default: break;
     }
     return best;

@@ -23,6 +23,7 @@ enum WaitSite : uint32_t {
     SITE_MMA_ACC_EMPTY = 3,
     SITE_EPI_ACC_FULL = 4,
     SITE_DRAIN = 5,
+    SITE_EPI_SPLIT = 6,
     SITE_SELFTEST = 9,
 };
 
@@ -170,6 +171,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to shared memory of another CTA of
+// the cluster (dst and the barrier in the shared::cluster window, from mapa;
+// 16-byte aligned, bytes a multiple of 16), completion counted on the
+// destination CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
         : "memory");
 }
 
@@ -403,21 +417,6 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta_
     return r;
 }
 
-__device__ __forceinline__ void dsmem_st_f4(uint32_t cluster_addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-
 // ---------------------------------------------------------------------------
 // Numerics shared by the epilogues.
 // ---------------------------------------------------------------------------
@@ -426,51 +425,118 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t cluster_addr) {
 // and Stegun, "Handbook of Mathematical Functions" (1964), formula 7.1.28:
 // for z >= 0,
 //     erfc(z) = 1 - erf(z) ~ (1 + a1 z + a2 z^2 + ... + a6 z^6)^-16,
-// absolute error at most 3e-7.  With z = |x| / sqrt 2 and r = erfc(z),
-// Phi(x) = 1 - r/2 for x >= 0 and r/2 for x < 0.  Cost: 6 fused
-// multiply-adds for the polynomial, 4 squarings, one hardware reciprocal.
-// The error of Phi stays near 1e-6 (the approximation plus the rounding of
-// the 16th power), three orders of magnitude below the half-ulp (2^-9
-// relative) of the bf16 value the epilogue stores.  For z above ~20 the
-// 16th power overflows to +inf and r = 0, the correct limit.
+// absolute error at most 3e-7.  With z = |x| / sqrt 2 and h = erfc(z) / 2,
+// Phi(x) = 1 - h for x >= 0 and h for x < 0, so
+//     GeLU(x) = max(x, 0) - |x| h.
+// The constants are folded into the polynomial: with u = -|x| and
+// k = 2^(1/16), P(u) = sum_i d_i u^i, d_i = k a_i (-1/sqrt 2)^i (d_0 = k),
+// equals k (1 + a1 z + ... + a6 z^6), so P^16 = 2 / erfc(z) and
+// h = 1 / P^16.  Cost per element: 6 fused multiply-adds, 4 squarings, one
+// hardware reciprocal, a max and a fused multiply-add; the packed variant
+// does two elements per fp32x2 instruction (fma.rn.f32x2 / mul.rn.f32x2,
+// each lane rounded exactly like the scalar fmaf / multiply, so both give
+// identical results).  The error stays below 1e-6 max(1, |x|) (the
+// approximation, the rounding of the 16th power and of the reciprocal),
+// three orders of magnitude below the half-ulp (2^-9 relative) of the bf16
+// value the epilogue stores.  For |x| above ~28 the 16th power overflows to
+// +inf and h = 0, the correct limit.
+constexpr float GELU_D0 = 1.04427373409271240e+00f;
+constexpr float GELU_D1 = -5.20751625299453735e-02f;
+constexpr float GELU_D2 = 2.20769979059696198e-02f;
+constexpr float GELU_D3 = -3.42273921705782413e-03f;
+constexpr float GELU_D4 = 3.96861360059119761e-05f;
+constexpr float GELU_D5 = -5.10552090418059379e-05f;
+constexpr float GELU_D6 = 5.62129980608006008e-06f;
+
 __device__ __forceinline__ float gelu_f32(float x) {
-    const float z = fabsf(x) * 0.70710678118654752440f;
-    float p = fmaf(4.30638e-5f, z, 2.765672e-4f);
-    p = fmaf(p, z, 1.520143e-4f);
-    p = fmaf(p, z, 9.2705272e-3f);
-    p = fmaf(p, z, 4.22820123e-2f);
-    p = fmaf(p, z, 7.05230784e-2f);
-    p = fmaf(p, z, 1.0f);
-    p = p * p;  // ^2
-    p = p * p;  // ^4
-    p = p * p;  // ^8
-    p = p * p;  // ^16
+    const float u = -fabsf(x);
+    float p = fmaf(GELU_D6, u, GELU_D5);
+    p = fmaf(p, u, GELU_D4);
+    p = fmaf(p, u, GELU_D3);
+    p = fmaf(p, u, GELU_D2);
+    p = fmaf(p, u, GELU_D1);
+    p = fmaf(p, u, GELU_D0);
+    p = __fmul_rn(p, p);  // ^2
+    p = __fmul_rn(p, p);  // ^4
+    p = __fmul_rn(p, p);  // ^8
+    p = __fmul_rn(p, p);  // ^16
     float h;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
-    h *= 0.5f;  // erfc(z) / 2
-    const float phi = x >= 0.0f ? 1.0f - h : h;
-    return x * phi;
+    return fmaf(u, h, fmaxf(x, 0.0f));
+}
+
+// Two fp32 values in one 64-bit register (lo in bits 0-31) and the packed
+// fp32x2 arithmetic of sm_100-class GPUs.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// gelu_f32 of two values at once (same operations, same results).
+__device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
+    const uint64_t u = f32x2_pack(-fabsf(x0), -fabsf(x1));
+    uint64_t p = fma_f32x2(f32x2_pack(GELU_D6, GELU_D6), u, f32x2_pack(GELU_D5, GELU_D5));
+    p = fma_f32x2(p, u, f32x2_pack(GELU_D4, GELU_D4));
+    p = fma_f32x2(p, u, f32x2_pack(GELU_D3, GELU_D3));
+    p = fma_f32x2(p, u, f32x2_pack(GELU_D2, GELU_D2));
+    p = fma_f32x2(p, u, f32x2_pack(GELU_D1, GELU_D1));
+    p = fma_f32x2(p, u, f32x2_pack(GELU_D0, GELU_D0));
+    p = mul_f32x2(p, p);
+    p = mul_f32x2(p, p);
+    p = mul_f32x2(p, p);
+    p = mul_f32x2(p, p);
+    float q0, q1, h0, h1;
+    f32x2_unpack(p, q0, q1);
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(q0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(q1));
+    const uint64_t y =
+        fma_f32x2(u, f32x2_pack(h0, h1), f32x2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)));
+    f32x2_unpack(y, x0, x1);
+}
+
+// GeLU of 32 values held as fp32 bit patterns (one tensor-memory load).
+__device__ __forceinline__ void gelu_chunk32(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+        gelu2_f32(a, b);
+        r[2 * i] = __float_as_uint(a);
+        r[2 * i + 1] = __float_as_uint(b);
+    }
 }
 
 // GeLU'(x) = Phi(x) + x * phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi), in fp32:
-// Phi from the same Abramowitz & Stegun 7.1.28 evaluation as gelu_f32, the
-// density from the hardware base-2 exponential (exp(-x^2/2) =
-// 2^(-x^2/2 * log2 e)).
+// Phi from the same folded Abramowitz & Stegun 7.1.28 polynomial as
+// gelu_f32 (Phi = 1 - h for x >= 0, h for x < 0), the density from the
+// hardware base-2 exponential (exp(-x^2/2) = 2^(-x^2/2 * log2 e)).
 __device__ __forceinline__ float gelu_grad_f32(float x) {
-    const float z = fabsf(x) * 0.70710678118654752440f;
-    float p = fmaf(4.30638e-5f, z, 2.765672e-4f);
-    p = fmaf(p, z, 1.520143e-4f);
-    p = fmaf(p, z, 9.2705272e-3f);
-    p = fmaf(p, z, 4.22820123e-2f);
-    p = fmaf(p, z, 7.05230784e-2f);
-    p = fmaf(p, z, 1.0f);
-    p = p * p;
-    p = p * p;
-    p = p * p;
-    p = p * p;
+    const float u = -fabsf(x);
+    float p = fmaf(GELU_D6, u, GELU_D5);
+    p = fmaf(p, u, GELU_D4);
+    p = fmaf(p, u, GELU_D3);
+    p = fmaf(p, u, GELU_D2);
+    p = fmaf(p, u, GELU_D1);
+    p = fmaf(p, u, GELU_D0);
+    p = __fmul_rn(p, p);
+    p = __fmul_rn(p, p);
+    p = __fmul_rn(p, p);
+    p = __fmul_rn(p, p);
     float h;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
-    h *= 0.5f;  // erfc(|x|/sqrt 2) / 2
     const float phi_cdf = x >= 0.0f ? 1.0f - h : h;
     float e;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * -0.72134752044448170368f));
