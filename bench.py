@@ -357,7 +357,7 @@ def run_ours(args):
 
     dom_ms, dom_flops, dom_name = ((k1_ms, flops_k1, "gemm column + GeLU (X.W1)")
                                    if k1_ms >= k2_ms else
-                                   (k2_ms, flops_k2, "gemm row + shard sum (H.W2)"))
+                                   (k2_ms, flops_k2, "gemm row, two-pair K split + shard sum in the cluster (H.W2)"))
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     # DRAM bytes per launch of the dominant kernel, from the committed capture
@@ -634,11 +634,21 @@ def bench_other_workloads(tp, torch, dev, stream, flush, peaks, K=20):
     Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
                      device=dev)
-    sweep = {}
-    for n in (1, 2, 4, 8, 16):
-        ms = _time_steps(torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush,
-                         stream, max(3, K // 2))
-        sweep[str(n)] = entry(ms, 4.0 * M * d * f)
+    # Every N runs the same two launches (the shards are logical partitions
+    # and the partial sums meet in the accumulator), so the N values are
+    # timed round-robin, three rounds, median per N: a long run of this size
+    # drifts down the clock (power cap), which would otherwise read as an
+    # effect of N.
+    shard_counts = (1, 2, 4, 8, 16)
+    times = {n: [] for n in shard_counts}
+    for _ in range(3):
+        for n in shard_counts:
+            times[n].append(_time_steps(
+                torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush, stream,
+                max(3, K // 4)))
+    sweep = {str(n): entry(sorted(times[n])[1], 4.0 * M * d * f) for n in shard_counts}
+    sweep["note"] = ("same launches for every N; N values timed round-robin, median of 3 rounds; "
+                     "differences between N are clock drift under the power cap")
     out["mlp_4096x8192x28672_sweep_n"] = sweep
     del X, W1, W2, Y, ws
     torch.cuda.synchronize()
