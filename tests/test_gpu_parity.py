@@ -530,6 +530,51 @@ def test_bias_integer_exact_and_empty(tp, cuda_device):
                                atol=4e-6)
 
 
+@pytest.mark.parametrize("M,K,N,n", [(300, 384, 400, 2), (513, 640, 272, 2)])
+def test_split_plan_paths(tp, cuda_device, M, K, N, n):
+    """The two-pair cluster split forced on every output path it has: an odd
+    k-block count (the two K halves differ in length), ragged M and N, bf16
+    output through TMA stores with bias and GeLU, the shard-major copy
+    (per-thread stores: must equal the plain output's columns bit for bit),
+    and fp32 output; integer-valued inputs give the exact product whatever
+    the order the two halves are added in."""
+    import torch
+    xb, wb = _bf16_inputs(M, K, N, seed=31 * M + N)
+    bb = inputs.bf16_normal((N,), inputs.stream_seed(31 * M + N, 7), 0.5)
+    X, W, b = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device), to_dev_bf16(bb, cuda_device)
+    Xd, Wd, bd = oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), oracle.bf16_to_f64(bb)
+    Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Ys = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+    Yc1 = torch.empty_like(Yc)
+    Yr = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    _with_plan("split2", lambda: tp.tp_column_linear_bias(X, W, b, Yc, Ys, n_shards=n, act="gelu"))
+    _with_plan("split2", lambda: tp.tp_column_linear_bias(X, W, b, Yc1, None, n_shards=n,
+                                                          act="gelu"))
+    _with_plan("split2", lambda: tp.tp_row_linear_bias(X, W, b, Yr, None, n_shards=n))
+    _status_ok(tp)
+    ref_c, ref_s = oracle.column_linear(Xd, Wd, n, act="gelu", bias=bd)
+    ref_r, _ = oracle.row_linear(Xd, Wd, n, bias=bd)
+    assert_bf16_parity(bf16_dev_to_f64(Yc), ref_c, "split: column + bias + GeLU, direct stores")
+    assert_bf16_parity(bf16_dev_to_f64(Yc1), ref_c, "split: column + bias + GeLU, TMA stores")
+    assert_bf16_parity(bf16_dev_to_f64(Yr), ref_r, "split: row + bias, bf16 out")
+    np.testing.assert_array_equal(dev_bits(Yc), dev_bits(Yc1))
+    ys = dev_bits(Ys)
+    yc = dev_bits(Yc)
+    for i in range(n):
+        np.testing.assert_array_equal(ys[i], yc[:, i * (N // n):(i + 1) * (N // n)])
+
+    xi = inputs.int_uniform((M, K), inputs.stream_seed(31 * M + N, 8))
+    wi = inputs.int_uniform((K, N), inputs.stream_seed(31 * M + N, 9))
+    Xi = to_dev_bf16(oracle.f64_to_bf16(xi), cuda_device)
+    Wi = to_dev_bf16(oracle.f64_to_bf16(wi), cuda_device)
+    exact = xi.astype(np.int64) @ wi.astype(np.int64)
+    for fn in (tp.tp_column_linear, tp.tp_row_linear):
+        Yf = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+        _with_plan("split2", lambda: fn(Xi, Wi, Yf, None, n_shards=n))
+        _status_ok(tp)
+        np.testing.assert_array_equal(dev_to_f64(Yf), exact)
+
+
 @pytest.mark.parametrize("M,d,f,n", [(200, 256, 512, 2), (2048, 1024, 4096, 2)])
 def test_mlp_block_bias(tp, cuda_device, M, d, f, n):
     import torch
