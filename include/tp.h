@@ -127,9 +127,10 @@ tp_status tp_column_linear_grouped(const void *X, const void *W, void *Y, void *
  * summed in ascending shard order in fp32.
  *   P_out == NULL: the partials are never materialised -- every shard's
  *     product is accumulated into the same fp32 tensor-memory accumulator
- *     (or, when the output has too few tiles to fill the GPU, shard groups
- *     run on the CTAs of one thread-block cluster and their fp32 partial
- *     tiles are added through distributed shared memory).  Y is required.
+ *     (or, when the output has too few tiles to fill the GPU, the first and
+ *     the second half of the shards are accumulated by the two CTA pairs of
+ *     one thread-block cluster and the two fp32 sums are added once,
+ *     exchanged between the pairs' shared memories).  Y is required.
  *   P_out != NULL: the fp32 partials are written to P_out [n_shards, M, Nout];
  *     if Y is also non-NULL it is then formed from them by tp_shard_reduce.
  * Errors: as tp_column_linear, with TP_ERR_DIVISIBILITY for K % n_shards.

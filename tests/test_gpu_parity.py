@@ -2,7 +2,7 @@
 oracle on the same seeded input bytes.  Sizes span several tiles with
 ragged tails in every dimension and exercise each kernel path (persistent
 tcgen05 GEMM with and without wrap-around, the cluster split with the
-distributed-shared-memory sum, per-shard partial outputs, the CUDA-core fp32
+shared-memory exchange of partial rows, per-shard partial outputs, the CUDA-core fp32
 path, the vector and scalar reduce, plain and head-group concat)."""
 import numpy as np
 import pytest
