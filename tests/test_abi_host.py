@@ -142,26 +142,3 @@ def test_mlp_validation(lib):
     assert mlp(Y=C) == ALIAS
     assert mlp(d=36) == ALIGN
     assert mlp(M=0) == OK
-
-
-def test_fast_division_formula():
-    """The concat kernel divides by invariant divisors with one
-    multiply-high; check the host magic + device formula on many values."""
-    def magic(d):
-        l = 0
-        while (1 << l) < d:
-            l += 1
-        m = ((1 << 32) * ((1 << l) - d)) // d + 1
-        return m & 0xFFFFFFFF, l
-
-    import random
-    rng = random.Random(1)
-    divisors = list(range(1, 300)) + [rng.randrange(1, 1 << 31) for _ in range(300)] + [1 << 30, (1 << 31) - 1]
-    for d in divisors:
-        m, s = magic(d)
-        for n in [0, 1, d - 1, d, d + 1, 2 * d - 1, (1 << 31) - 1] + [rng.randrange(0, 1 << 31) for _ in range(50)]:
-            if n < 0 or n >= (1 << 31):
-                continue
-            hi = (n * m) >> 32
-            q = ((hi + n) & 0xFFFFFFFF) >> s
-            assert q == n // d, (n, d)
