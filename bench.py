@@ -503,16 +503,44 @@ def whole_job_rate(work_per_rank_step, ms_per_step_max, world):
     return world * work_per_rank_step / (ms_per_step_max * 1e-3)
 
 
+def _code_only(src):
+    """C++ source without its comments and with every run of white space
+    collapsed to one blank: what the compiler sees, so that editing a comment
+    does not change the hash below.  String and character literals are kept
+    verbatim (inline PTX lives in them)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha():
-    """Short hash of the CUDA sources, to tie profiler counters to a build."""
+    """Short hash of the CUDA sources' code (comments and layout ignored), to
+    tie profiler counters to the kernels they were taken on."""
     import glob
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_sharded_linear_02_b300", "csrc")
     for f in sorted(glob.glob(os.path.join(csrc, "*.cuh")) + [os.path.join(csrc, "tp_api.cu")]):
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -4,7 +4,7 @@
 //   A  row-major [M, K]   (X, or the hidden activation H)  -> K-major operand
 //   B  row-major [K, N]   (the weight W as stored)          -> MN-major operand
 //
-// Every kernel runs on CTA pairs (clusters of 2, or of 2*S for the split
+// Every kernel runs on CTA pairs (clusters of 2, or of 4 for the split
 // kernel) and issues tcgen05.mma.cta_group::2: one 256 x bn output tile per
 // pair (bn = 256 or 128), 256 x bn x 16 per instruction.  The even CTA of a
 // pair stages A rows 0..127 and B columns 0..bn/2-1 of the tile, the odd CTA
@@ -21,16 +21,16 @@
 // both CTAs are counted on the even CTA's `full` barrier; one thread of the
 // even CTA issues the MMAs and releases a stage in both CTAs with a multicast
 // commit; the epilogue warps of each CTA read its own TMEM (tcgen05.ld),
-// apply the optional GeLU, round to bf16 (RNE) or keep fp32, and write
-// through swizzled shared-memory boxes and TMA stores.
+// add the optional bias, apply the optional GeLU, round to bf16 (RNE) or
+// keep fp32, and write through swizzled shared-memory boxes and TMA stores.
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner (and
 // MMA issuer in the even CTA), warps 2..9 = epilogue (warp w reads TMEM lanes
 // 32*(w%4)..+31; warps 2..5 take the first half of the accumulator columns,
 // warps 6..9 the second half).
 //
-// The tile width is a per-unit run-time value no larger than the ring's
-// template width, so one kernel can mix 256- and 128-wide tiles.
+// The tile width of a launch (256 or 128) is a run-time value no larger than
+// the ring's template width.
 //
 // Kernels:
 //   gemm_persistent_kernel<MAXBN>  one pair per two SMs walks work units

@@ -60,3 +60,18 @@ def test_reference_arm_line():
     assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_source_hash_ignores_comments_only():
+    """The hash that ties committed profiler counters to the kernels drops
+    comments and layout but keeps code and string literals (inline PTX)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int x = 1; // note\nasm("mov.u32 %0, 1; // not a comment");\n'
+    b = 'int x = 1;   /* other\nnote */\nasm("mov.u32 %0, 1; // not a comment");'
+    c = 'int x = 2; // note\nasm("mov.u32 %0, 1; // not a comment");\n'
+    d = 'int x = 1; // note\nasm("mov.u32 %0, 2; // not a comment");\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only(a) != bench._code_only(d)
+    assert bench._code_only("char q = '\"'; // x") == "char q = '\"';"
