@@ -109,7 +109,17 @@ def _dtype_code(t) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a tensor the C ABI reads as a dense row-major array:
+    a CPU tensor or a strided view (a transpose, a column slice) would be
+    misread, so both are refused here."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"tensor of shape {tuple(t.shape)} is not on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {t.stride()} is not "
+                         f"contiguous (row-major)")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):

@@ -142,3 +142,14 @@ def test_mlp_validation(lib):
     assert mlp(Y=C) == ALIAS
     assert mlp(d=36) == ALIGN
     assert mlp(M=0) == OK
+
+
+def test_binding_refuses_host_tensors():
+    """The binding hands the C ABI device pointers only: a CPU tensor is
+    refused before any call."""
+    import torch
+    X = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(8, 16, dtype=torch.bfloat16)
+    Y = torch.zeros(4, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.tp_column_linear(X, W, Y, None, n_shards=2)

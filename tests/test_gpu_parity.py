@@ -530,6 +530,20 @@ def test_bias_integer_exact_and_empty(tp, cuda_device):
                                atol=4e-6)
 
 
+def test_binding_refuses_strided_views(tp, cuda_device):
+    """A transposed or column-sliced view is not the dense row-major array
+    the C ABI reads: the binding refuses it instead of misreading it."""
+    import torch
+    X = torch.zeros(64, 32, dtype=torch.bfloat16, device=cuda_device)
+    Wt = torch.zeros(64, 32, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.zeros(32, 32, dtype=torch.bfloat16, device=cuda_device)
+    Y = torch.zeros(64, 64, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(ValueError, match="contiguous"):
+        tp.tp_column_linear(X, Wt.t(), Y, None, n_shards=2)  # W as a transposed view
+    with pytest.raises(ValueError, match="contiguous"):
+        tp.tp_column_linear(X, W, Y[:, :32], None, n_shards=2)  # Y as a column slice
+
+
 @pytest.mark.parametrize("M,K,N,n", [(300, 384, 400, 2), (513, 640, 272, 2)])
 def test_split_plan_paths(tp, cuda_device, M, K, N, n):
     """The two-pair cluster split forced on every output path it has: an odd
