@@ -5,26 +5,35 @@ concat) on B300, printing one JSON line.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
 
-Default workload: the Megatron MLP block with X [2048, 1024] ~ N(0,1),
-W1 [1024, 4096] and W2 [4096, 1024] ~ N(0, 0.02), N = 2 logical shards
-(column GEMM + exact GeLU, row GEMM with the shard sum in the accumulator).
-A step is one tp_mlp_block call.  Its working set (about 40 MB) fits in the
-126 MB L2, so L2 is flushed (a 256 MB device write) before every timed step,
-outside the timed interval.  Each step is timed with CUDA events on the
-launching stream; the sum over K steps is the device time.
+Default workload: the wide MLP block, the largest one that the method's
+workloads run on one GPU: X [4096, 8192] ~ N(0,1), W1 [8192, 28672] and
+W2 [28672, 8192] ~ N(0, 0.01), N = 8 logical shards (column GEMM + exact
+GeLU, row GEMM with the shard sum in the accumulator; 3.85 TFLOP per step).
+A step is one tp_mlp_block call.  L2 is flushed (a 256 MB device write)
+before every timed step, outside the timed interval.  Each step is timed
+with CUDA events on the launching stream; the sum over K steps is the
+device time.
 
 Also reported on the same line:
   roofline      the dominant kernel of the step (per-kernel event timing of
-                the same two launches) against the measured bf16 peak
+                the same two launches) against the measured bf16 burst peak,
+                with its DRAM bytes per launch from the committed capture
+  mlp_small     the small MLP block (2048 x 1024 x 4096, N = 2): block time,
+                per-kernel split and roofline
   reduce        the standalone shard reduce, N = 8 fp32 partials
-                [8, 4096, 8192] -> bf16 (1.14 GB per launch, larger than L2)
+                [8, 4096, 8192] -> bf16 (1.14 GB per launch, larger than L2),
+                and its sweep over N = 1, 2, 4, 8, 16
   concat        the standalone head-group concat, 8 x [8192, 1536] bf16 ->
                 [8192, 12288] (Q|K|V blocks)
+  backward      the MLP backward step on the GPT MLP (4096 x 4096 x 16384,
+                N = 8) and the small MLP, with per-launch figures
+  other_workloads  GPT MLP block, attention projections, the wide MLP for
+                N = 1 .. 16
   e2e           the same MLP metric through the C ABI with the input copied
                 from pinned host memory and the output copied back, per step
-  cpu_baseline  the fp64 oracle on the host cores, same workload
-  clocks        SM clock and throttle reasons sampled through NVML during the
-                timed region
+  cpu_baseline  the fp64 oracle on the host cores, on a sample of the
+                workload's rows
+  clocks        SM clock and throttle reasons sampled during the timed region
 
 --impl reference times the oracle (plain fp64 host C) on a bounded sample of
 the same workload, as the reference arm.
@@ -51,7 +60,7 @@ WORKLOADS = {
     "mlp_4096x4096x16384_n8": (4096, 4096, 16384, 8, 0.02),
     "mlp_4096x8192x28672_n8": (4096, 8192, 28672, 8, 0.01),
 }
-DEFAULT_WORKLOAD = "mlp_2048x1024x4096_n2"
+DEFAULT_WORKLOAD = "mlp_4096x8192x28672_n8"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -249,6 +258,75 @@ def _host_cores():
 
 # --------------------------------------------------------- our arm ---------
 
+def _kernel_split(tp, torch, X, W1, W2, H, Y, n, flush, stream, K):
+    """Mean event time (ms) of the column GEMM + GeLU and of the row GEMM +
+    shard sum: the same two launches as tp_mlp_block, with an event between
+    them, L2 flushed before each pair."""
+    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    for i in range(K):
+        _prequeue(torch, i)
+        flush.zero_()
+        ev3[i][0].record(stream)
+        tp.tp_column_linear(X, W1, H, None, n_shards=n, act="gelu")
+        ev3[i][1].record(stream)
+        tp.tp_row_linear(H, W2, Y, None, n_shards=n)
+        ev3[i][2].record(stream)
+    torch.cuda.synchronize()
+    k1_ms = sum(a.elapsed_time(b) for a, b, _ in ev3) / K
+    k2_ms = sum(b.elapsed_time(c) for _, b, c in ev3) / K
+    return k1_ms, k2_ms
+
+
+def _gemm_roofline(workload, k1_ms, k2_ms, flops_k1, flops_k2, peaks):
+    """Roofline block for the dominant GEMM of an MLP step (tensor-bound):
+    algorithmic FLOPs per launch (2 M K N) over its mean event time, against
+    the measured burst bf16 peak; DRAM traffic per launch from the committed
+    capture of this workload (null if the kernels changed since)."""
+    col = k1_ms >= k2_ms
+    dom_ms, dom_flops = (k1_ms, flops_k1) if col else (k2_ms, flops_k2)
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = _profile_traffic(workload, "column_gemm_bytes" if col else "bytes")
+    return {"bound": "tensor",
+            "kernel": "gemm column + GeLU (X.W1)" if col else
+                      "gemm row + shard sum in the accumulator (H.W2)",
+            "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "flops_per_launch": dom_flops,
+            "peak_source": peaks["source"] + " burst bf16",
+            "kernel_ms": {"gemm_column_gelu": round(k1_ms, 5),
+                          "gemm_row_shard_sum": round(k2_ms, 5)},
+            "kernel_frac": {"gemm_column_gelu": round(flops_k1 / (k1_ms * 1e-3) / 1e12 / peak, 4),
+                            "gemm_row_shard_sum": round(flops_k2 / (k2_ms * 1e-3) / 1e12 / peak,
+                                                        4)}}
+
+
+def _oracle_sample(xb, w1b, w2b, n, seconds):
+    """The oracle as it stands on the first R rows of the workload, R sized
+    from a 4-row calibration so that the passes take about `seconds` of
+    host time (each output row depends only on its own input row, so the
+    rate on R rows is the rate on the whole workload)."""
+    import oracle
+    W1, W2 = oracle.bf16_to_f64(w1b), oracle.bf16_to_f64(w2b)
+    d, f = W1.shape
+    t0 = time.perf_counter()
+    oracle.mlp_block(oracle.bf16_to_f64(xb[:4]), W1, W2, n)
+    per_row = (time.perf_counter() - t0) / 4
+    rows = int(max(4, min(xb.shape[0], seconds / 2 / max(per_row, 1e-9))))
+    X = oracle.bf16_to_f64(xb[:rows])
+    times = []
+    while sum(times) < seconds / 2 or len(times) < 2:
+        t0 = time.perf_counter()
+        oracle.mlp_block(X, W1, W2, n)
+        times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    flops = 2.0 * rows * d * f * 2
+    return {"value": flops / mean / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
+            "kind": "oracle",
+            "sample": f"first {rows} of {xb.shape[0]} rows, fp64 naive loops, {len(times)} "
+                      f"passes, {sum(times):.1f} s, mean {mean:.2f} s per pass"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -312,57 +390,36 @@ def run_ours(args):
         raise RuntimeError("device status error in the timed region")
 
     # per-kernel attribution: the same two GEMM launches with an event between
-    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
-    for i in range(K):
-        _prequeue(torch, i)
-        flush.zero_()
-        ev3[i][0].record(stream)
-        tp.tp_column_linear(X, W1, H, None, n_shards=n, act="gelu")
-        ev3[i][1].record(stream)
-        tp.tp_row_linear(H, W2, Y, None, n_shards=n)
-        ev3[i][2].record(stream)
-    torch.cuda.synchronize()
-    k1_ms = sum(a.elapsed_time(b) for a, b, _ in ev3) / K
-    k2_ms = sum(b.elapsed_time(c) for _, b, c in ev3) / K
+    k1_ms, k2_ms = _kernel_split(tp, torch, X, W1, W2, H, Y, n, flush, stream, K)
+    roofline = _gemm_roofline(args.workload, k1_ms, k2_ms, flops_k1, flops_k2, peaks)
 
-    # -------------------------------------------------- standalone reduce ---
-    red = cat = None
+    # --------------------------------------------------------------- e2e ----
+    Ke = min(K, 200) if not args.skip_extras else 3
+    e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
+
+    # ------------------------------------------------------------- extras ----
+    red = cat = bwd = others = small = None
     if not args.skip_extras:
+        small = bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=min(max(K, 200), 2000))
         red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
         red["sweep"] = {str(ns): bench_reduce(tp, dev, stream, peaks, K=min(K, 100), n=ns)["value"]
                         for ns in (1, 2, 4, 16)}
         red["sweep"]["8"] = red["value"]
+        red["sweep_frac"] = {k: round(v / peaks["hbm_gbs"], 4) for k, v in red["sweep"].items()}
         cat = bench_concat(tp, dev, stream, peaks, K=min(K, 200))
-
-    # ----------------------------------------------------------- backward ----
-    bwd = None
-    if not args.skip_extras:
-        bwd = bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks,
-                             K=min(K, 200))
-
-    # ------------------------------------------------- the other workloads ----
-    others = None
-    if not args.skip_extras:
+        del X, W1, W2, Y, ws, H
+        bwd = bench_backward_workload(tp, torch, dev, stream, flush, peaks,
+                                      "mlp_4096x4096x16384_n8", K=min(K, 20))
+        bwd_small = bench_backward_workload(tp, torch, dev, stream, flush, peaks,
+                                            "mlp_2048x1024x4096_n2", K=min(max(K, 100), 500))
+        bwd = {"mlp_4096x4096x16384_n8": bwd, "mlp_2048x1024x4096_n2": bwd_small}
         others = bench_other_workloads(tp, torch, dev, stream, flush, peaks, K=min(K, 20))
-
-    # --------------------------------------------------------------- e2e ----
-    Ke = min(K, 500) if not args.skip_extras else 3
-    e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
 
     # --------------------------------------------------- max over ranks -----
     dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], dev, world)
     ms_per_step = dev_ms / K
     value = whole_job_rate(flops_step, ms_per_step, world) / 1e12
     e2e_value = whole_job_rate(flops_step, e2e_ms, world) / 1e12
-
-    dom_ms, dom_flops, dom_name = ((k1_ms, flops_k1, "gemm column + GeLU (X.W1)")
-                                   if k1_ms >= k2_ms else
-                                   (k2_ms, flops_k2, "gemm row, two-pair K split + shard sum in the cluster (H.W2)"))
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
-    # DRAM bytes per launch of the dominant kernel, from the committed capture
-    traffic = _profile_traffic(args.workload,
-                               "bytes" if dom_name.startswith("gemm row") else "column_gemm_bytes")
 
     if rank != 0:
         if world > 1:
@@ -371,18 +428,10 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and not args.skip_extras and world == 1:
-        # the oracle as it stands, on the whole workload, repeated until about
-        # 10 s of host time have passed
-        flops_s, times = cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)
-        while sum(times) < 10.0:
-            times += cpu_oracle_mlp(xb, w1b, w2b, n, rows=M, repeats=1)[1]
-        mean = sum(times) / len(times)
-        cpu = {"value": flops_s / mean / 1e12, "unit": "TFLOP/s", "cores": _host_cores(),
-               "kind": "oracle",
-               "sample": f"full workload ({M} rows), fp64 naive loops, {len(times)} passes, "
-                         f"{sum(times):.1f} s, mean {mean:.2f} s per pass"}
+        cpu = _oracle_sample(xb, w1b, w2b, n, seconds=20.0)
 
     clocks = clk.summary()
+    peak = peaks["bf16_tflops"]
     line = {
         "metric": "sharded MLP-block TFLOP/s on 1 B300 (% bf16 dense peak); shard-reduce HBM GB/s",
         "value": round(value, 2),
@@ -401,11 +450,8 @@ def run_ours(args):
                    "l2": "flushed before every timed step (256 MB write)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "frac_of_peak": round(value / peak, 4),
-        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 2),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": peaks["source"] + " burst bf16",
-                     "kernel_ms": {"gemm_column_gelu": round(k1_ms, 5),
-                                   "gemm_row_shard_sum": round(k2_ms, 5)}},
+        "roofline": roofline,
+        "mlp_small": small,
         "reduce": red,
         "concat": cat,
         "backward": bwd,
@@ -425,6 +471,31 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=2000):
+    """The small MLP block (X [2048, 1024], W1 [1024, 4096], W2 [4096, 1024],
+    N = 2; about 40 MB, inside L2, hence the flush before every step):
+    block time, per-kernel split and the dominant kernel's roofline."""
+    name = "mlp_2048x1024x4096_n2"
+    M, d, f, n, std = WORKLOADS[name]
+    xb, w1b, w2b = _make_mlp_inputs(M, d, f, std, dev)
+    X, W1, W2 = _bf16_dev(xb, dev), _bf16_dev(w1b, dev), _bf16_dev(w2b, dev)
+    Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    H = ws[: M * f * 2].view(torch.bfloat16).view(M, f)
+    ms = _time_steps(torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush, stream,
+                     K)
+    k1_ms, k2_ms = _kernel_split(tp, torch, X, W1, W2, H, Y, n, flush, stream, K)
+    flops = 2.0 * M * d * f
+    tf = 2 * flops / (ms * 1e-3) / 1e12
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the small MLP block")
+    return {"workload": name, "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "steps": K, "roofline": _gemm_roofline(name, k1_ms, k2_ms, flops, flops, peaks),
+            "l2": "flushed before every timed step (256 MB write)"}
 
 
 PREQUEUE_BATCH = 20
@@ -558,39 +629,57 @@ def _profile_traffic(workload, field="bytes"):
     return entry.get(field)
 
 
-def bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks, K=200):
-    """tp_mlp_block_backward on the bench workload (dY ~ N(0,1) synthetic).
-    Counted work: the four products of the backward pass, 4 * 2*M*d*f (the
-    recomputation of the pre-activation, a fifth product, is not counted)."""
-    from tensor_sharded_linear_02_b300 import inputs
-    dY = _bf16_dev(inputs.bf16_normal((M, d), inputs.stream_seed(1, 3), 1.0), X.device)
+def bench_backward_workload(tp, torch, dev, stream, flush, peaks, name, K=20):
+    """tp_mlp_block_backward on an MLP workload (inputs from a seeded device
+    generator, dY ~ N(0, 1)).  Counted work: the four products of the
+    backward pass, 4 * 2*M*d*f (the recomputation of the pre-activation, a
+    fifth product, is not counted).  Per launch: the three gradient products
+    that the linears' backward entry points run alone (same shapes, same
+    kernels, one launch each) are timed on their own; the remaining two
+    launches of the step (pre-activation recompute with the dual epilogue,
+    dZ with the GeLU' epilogue) are the step time minus those three."""
+    M, d, f, n, std = WORKLOADS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(20261203)
+
+    def bf(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    X, W1, W2, dY = bf(M, d), bf(d, f, s=std), bf(f, d, s=std), bf(M, d)
     ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
-                     dtype=torch.uint8, device=X.device)
-    dX = torch.empty(M, d, dtype=torch.bfloat16, device=X.device)
-    dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=X.device)
-    dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=X.device)
-
-    def step():
-        tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
-
-    for _ in range(5):
-        step()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    torch.cuda.synchronize()
-    for i in range(K):
-        _prequeue(torch, i)
-        flush.zero_()
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    flops = 4 * 2.0 * M * d * f
-    tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": f"MLP block backward, same sizes, N={n}", "value": round(tf, 2),
-            "unit": "TFLOP/s", "ms_per_step": round(ms, 5), "flops_per_step": flops,
-            "launches_per_step": 5, "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+                     dtype=torch.uint8, device=dev)
+    dX = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=dev)
+    ms = _time_steps(torch, lambda: tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2,
+                                                             n_shards=n), flush, stream, K)
+    part = (M * f * 2 + 255) // 256 * 256
+    H = ws[part: part + M * f * 2].view(torch.bfloat16).view(M, f)
+    dZ = ws[2 * part: 2 * part + M * f * 2].view(torch.bfloat16).view(M, f)
+    t = {
+        "dW2 = H^T.dY": _time_steps(torch, lambda: tp.tp_row_linear_backward(
+            H, W2, dY, None, dW2, n_shards=n), flush, stream, K),
+        "dW1 = X^T.dZ": _time_steps(torch, lambda: tp.tp_column_linear_backward(
+            X, W1, dZ, None, dW1, n_shards=n), flush, stream, K),
+        "dX = dZ.W1^T": _time_steps(torch, lambda: tp.tp_column_linear_backward(
+            X, W1, dZ, dX, None, n_shards=n), flush, stream, K),
+    }
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the backward pass")
+    gemm = 2.0 * M * d * f
+    peak = peaks["bf16_tflops"]
+    per = {k: {"ms": round(v, 5), "tflops": round(gemm / (v * 1e-3) / 1e12, 1),
+               "frac": round(gemm / (v * 1e-3) / 1e12 / peak, 4)} for k, v in t.items()}
+    rest = ms - sum(t.values())
+    per["Z, H recompute + dZ = (dY.W2^T) * GeLU'(Z) (2 launches)"] = {
+        "ms": round(rest, 5), "tflops": round(2 * gemm / (rest * 1e-3) / 1e12, 1),
+        "frac": round(2 * gemm / (rest * 1e-3) / 1e12 / peak, 4)}
+    tf = 4 * gemm / (ms * 1e-3) / 1e12
+    return {"workload": f"MLP block backward {name}", "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "flops_per_step": 4 * gemm, "launches_per_step": 5,
+            "frac_of_peak": round(tf / peak, 4),
+            "tflops_all_5_products": round(5 * gemm / (ms * 1e-3) / 1e12, 2),
+            "per_launch": per,
             "note": "dX, dW1, dW2 (bf16) with the pre-activation recomputed; L2 flushed "
                     "before every step; counted work excludes the recomputation"}
 
@@ -690,12 +779,14 @@ def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
     from tensor_sharded_linear_02_b300 import inputs
     P = torch.from_numpy(inputs.f32_normal((n, rows, cols), 4242)).to(dev)
     Y = torch.empty(rows, cols, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(5):
         tp.tp_shard_reduce(P, Y)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
+        flush.zero_()
         ev[i][0].record(stream)
         tp.tp_shard_reduce(P, Y)
         ev[i][1].record(stream)
@@ -709,7 +800,7 @@ def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": _profile_traffic(f"reduce_{n}x{rows}x{cols}"),
                          "peak_source": peaks["source"] + " copy bandwidth"},
-            "l2": "inputs (1.07 GB) larger than L2"}
+            "l2": "flushed before every timed launch (256 MB write)"}
 
 
 def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=3):
@@ -742,7 +833,13 @@ def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=
 
 
 def run_leg(args):
-    """A few launches of one standalone kernel at its bench workload."""
+    """A few launches of one kernel or step at its bench workload, printing
+    nothing (for profiler captures):
+      reduce    the standalone shard reduce, N fp32 partials [4096, 8192]
+                (--reduce-n)
+      concat    the standalone head-group concat
+      backward  the MLP backward step of --workload
+      gemm      the MLP block of --workload (column GEMM + GeLU, row GEMM)"""
     import torch
     from tensor_sharded_linear_02_b300 import binding as tp
     dev = torch.device("cuda", 0)
@@ -750,16 +847,25 @@ def run_leg(args):
     stream = torch.cuda.current_stream()
     peaks = _peaks()
     K = max(1, args.steps)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.leg == "reduce":
-        bench_reduce(tp, dev, stream, peaks, K=K)
+        bench_reduce(tp, dev, stream, peaks, K=K, n=args.reduce_n)
     elif args.leg == "concat":
         bench_concat(tp, dev, stream, peaks, K=K)
+    elif args.leg == "backward":
+        bench_backward_workload(tp, torch, dev, stream, flush, peaks, args.workload, K=K)
     else:
         M, d, f, n, std = WORKLOADS[args.workload]
-        xb, w1b, w2b = _make_mlp_inputs(M, d, f, std, dev)
-        X, W1, W2 = _bf16_dev(xb, dev), _bf16_dev(w1b, dev), _bf16_dev(w2b, dev)
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        bench_backward(tp, torch, X, W1, W2, M, d, f, n, flush, stream, peaks, K=K)
+        g = torch.Generator(device=dev)
+        g.manual_seed(20261204)
+        X = (torch.randn(M, d, generator=g, device=dev)).to(torch.bfloat16)
+        W1 = (torch.randn(d, f, generator=g, device=dev) * std).to(torch.bfloat16)
+        W2 = (torch.randn(f, d, generator=g, device=dev) * std).to(torch.bfloat16)
+        Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16), dtype=torch.uint8,
+                         device=dev)
+        _time_steps(torch, lambda: tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n), flush, stream,
+                    K)
     torch.cuda.synchronize()
     if tp.tp_get_device_status() != tp.TP_OK:
         raise RuntimeError("device status error")
@@ -817,14 +923,16 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--leg", choices=["reduce", "concat", "backward"], default=None,
-                    help="run only a few launches of one standalone kernel at its bench "
+    ap.add_argument("--leg", choices=["reduce", "concat", "backward", "gemm"], default=None,
+                    help="run only a few launches of one kernel or step at its bench "
                          "workload and print nothing else (for profiler captures)")
+    ap.add_argument("--reduce-n", type=int, default=8,
+                    help="shard count of the reduce leg")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the MLP step (for profiler captures)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,

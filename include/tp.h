@@ -38,6 +38,9 @@
  *     with exact fp32 fused multiply-adds in ascending k (bit-exact for
  *     integer-valued data whose sums stay below 2^24); it needs only 4-byte
  *     alignment.  M may be anything >= 0.
+ *   - Each of M, K, Nout (d, f) is at most 2^31 - 1 and each matrix holds at
+ *     most 2^40 elements; larger sizes return TP_ERR_SHAPE (the workspace
+ *     size queries return 0 for them).
  *   - Outputs must not overlap inputs (TP_ERR_ALIAS).
  *   - Device-side waits are bounded; a wait that runs out marks the device
  *     status word, read back with tp_get_device_status().
@@ -56,7 +59,9 @@ extern "C" {
 typedef enum {
     TP_OK = 0,
     TP_ERR_NULL = 1,          /* a required pointer is NULL */
-    TP_ERR_SHAPE = 2,         /* negative size, or sizes inconsistent */
+    TP_ERR_SHAPE = 2,         /* negative size, sizes inconsistent, a size
+                                 above 2^31 - 1, or a matrix of more than
+                                 2^40 elements */
     TP_ERR_DIVISIBILITY = 3,  /* the split axis is not divisible by n_shards
                                  (or by col_groups), or n_shards out of range */
     TP_ERR_ALIGNMENT = 4,     /* pointer or row pitch not aligned as required */

@@ -29,6 +29,9 @@ the design notes):
 * Partials are summed in ascending shard order.
 * Head-group split for the QKV projection: columns form G blocks (Q|K|V) and
   shard i owns the i-th contiguous slice of each block.
+* Sequence parallelism: shard i owns token rows [i*M/n, (i+1)*M/n) outside
+  the tensor-parallel block; after the block's all-reduce each shard keeps
+  its own token rows (a reduce-scatter over token rows).
 
 Parity pins for each function are in ``tests/test_oracle_pins.py``.
 """
@@ -103,6 +106,9 @@ def _load():
                                                _i64, _i64]
         lib.orc_shard_reduce.argtypes = [_fp, _dp, _i64, _i64, _i64]
         lib.orc_shard_concat.argtypes = [_dp, _dp, _i64, _i64, _i64, _i64]
+        lib.orc_allgather_rows.argtypes = [_dp, _dp, _i64, _i64, _i64]
+        lib.orc_reduce_scatter_rows.argtypes = [_dp, _dp, _i64, _i64, _i64]
+        lib.orc_seq_parallel_mlp_block.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
         _lib = lib
         return lib
 
@@ -311,3 +317,43 @@ def shard_concat(Ys, col_groups: int = 1) -> np.ndarray:
     Y = np.empty((rows, n * sc), dtype=np.float64)
     _load().orc_shard_concat(_ptr(Ys), _ptr(Y), rows, sc, n, col_groups)
     return Y
+
+
+# ------------------------------------------------- sequence parallelism ----
+
+def allgather_rows(Xs) -> np.ndarray:
+    """All-gather of token blocks before the tensor-parallel block
+    ([TP-topic] "Sequence Parallelism Extension": every shard needs every
+    token): Xs [n, M/n, cols] -> X [M, cols], shard i's rows i*M/n onward."""
+    Xs = _f64(Xs)
+    n, rb, cols = Xs.shape
+    X = np.empty((n * rb, cols), dtype=np.float64)
+    _load().orc_allgather_rows(_ptr(Xs), _ptr(X), n, rb, cols)
+    return X
+
+
+def reduce_scatter_rows(P) -> np.ndarray:
+    """The combine after the block under sequence parallelism ([TP-topic]
+    "Sequence Parallelism Extension"): the all-reduce of the shards'
+    partial outputs P [n, M, cols] (ascending shard order), after which
+    shard i keeps its own token rows: returns [n, M/n, cols]."""
+    P = _f64(P)
+    n, M, cols = P.shape
+    assert M % n == 0
+    Ys = np.empty((n, M // n, cols), dtype=np.float64)
+    _load().orc_reduce_scatter_rows(_ptr(P), _ptr(Ys), n, M, cols)
+    return Ys
+
+
+def seq_parallel_mlp_block(Xs, W1, W2) -> np.ndarray:
+    """MLP block between two sequence-split regions: token blocks
+    Xs [n, M/n, d] are all-gathered, every shard i computes its partial
+    GeLU(X.W1_i).W2_i for all tokens, and the partials are reduce-scattered
+    over token rows: returns [n, M/n, d]."""
+    Xs, W1, W2 = _f64(Xs), _f64(W1), _f64(W2)
+    n, rb, d = Xs.shape
+    _, f = W1.shape
+    assert W1.shape == (d, f) and W2.shape == (f, d) and f % n == 0
+    Ys = np.empty((n, rb, d), dtype=np.float64)
+    _load().orc_seq_parallel_mlp_block(_ptr(Xs), _ptr(W1), _ptr(W2), _ptr(Ys), n, rb, d, f)
+    return Ys

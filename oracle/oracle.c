@@ -479,3 +479,71 @@ void orc_shard_concat(const double *Ys, double *Y, int64_t rows, int64_t shard_c
                 for (int64_t j = 0; j < sw; ++j)
                     Y[r * N + b * gw + i * sw + j] = Ys[(i * rows + r) * shard_cols + b * sw + j];
 }
+
+/* ------------------------------------------------------------------------ */
+/* Sequence parallelism ([TP-topic] "Sequence Parallelism Extension"):       */
+/* outside the tensor-parallel block the token (sequence) dimension is split */
+/* across the shards, each holding a contiguous subset of the token rows;    */
+/* before the block the token subsets are all-gathered (every shard needs    */
+/* every token), and after it the shards' partial outputs are all-reduced.  */
+/* Reading: after the all-reduce each shard keeps only its own token subset */
+/* for the sequence-split part that follows, so the combine is "sum over    */
+/* shards, then split by token rows" (a reduce-scatter over token rows).    */
+/* Shard i owns token rows [i*Mb, (i+1)*Mb), Mb = M / n.                    */
+/* ------------------------------------------------------------------------ */
+
+/* All-gather of token blocks: Xs [n][Mb][cols] -> X [n*Mb][cols]. */
+void orc_allgather_rows(const double *Xs, double *X, int64_t n_shards, int64_t rows_per_shard,
+                        int64_t cols)
+{
+    for (int64_t i = 0; i < n_shards; ++i)
+        for (int64_t r = 0; r < rows_per_shard; ++r)
+            for (int64_t c = 0; c < cols; ++c)
+                X[(i * rows_per_shard + r) * cols + c] = Xs[(i * rows_per_shard + r) * cols + c];
+}
+
+/* Reduce-scatter over token rows: P [n][M][cols] (shard j's partial output  */
+/* for every token) -> Ys [n][M/n][cols], Ys[i] = token rows of shard i of  */
+/* sum_j P_j, the sum over ascending j (the all-reduce), then the split.    */
+void orc_reduce_scatter_rows(const double *P, double *Ys, int64_t n_shards, int64_t M,
+                             int64_t cols)
+{
+    const int64_t Mb = M / n_shards;
+    double *S = (double *)malloc(sizeof(double) * (size_t)(M * cols > 0 ? M * cols : 1));
+    for (int64_t t = 0; t < M * cols; ++t) {            /* all-reduce */
+        double acc = 0.0;
+        for (int64_t j = 0; j < n_shards; ++j)
+            acc += P[j * M * cols + t];
+        S[t] = acc;
+    }
+    for (int64_t i = 0; i < n_shards; ++i)             /* keep own token rows */
+        for (int64_t r = 0; r < Mb; ++r)
+            for (int64_t c = 0; c < cols; ++c)
+                Ys[(i * Mb + r) * cols + c] = S[(i * Mb + r) * cols + c];
+    free(S);
+}
+
+/* MLP block between two sequence-split regions: token blocks Xs [n][Mb][d] */
+/* -> all-gather -> per shard i: P_i = GeLU(X . W1_i) . W2_i for every token */
+/* -> reduce-scatter over token rows -> Ys [n][Mb][d].                       */
+void orc_seq_parallel_mlp_block(const double *Xs, const double *W1, const double *W2,
+                                double *Ys, int64_t n_shards, int64_t rows_per_shard, int64_t d,
+                                int64_t f)
+{
+    const int64_t M = n_shards * rows_per_shard, fs = f / n_shards;
+    double *X = (double *)malloc(sizeof(double) * (size_t)(M * d > 0 ? M * d : 1));
+    double *W1i = (double *)malloc(sizeof(double) * (size_t)(d * fs > 0 ? d * fs : 1));
+    double *Hi = (double *)malloc(sizeof(double) * (size_t)(M * fs > 0 ? M * fs : 1));
+    double *P = (double *)malloc(sizeof(double) * (size_t)(n_shards * M * d > 0 ? n_shards * M * d : 1));
+    orc_allgather_rows(Xs, X, n_shards, rows_per_shard, d);
+    for (int64_t i = 0; i < n_shards; ++i) {
+        for (int64_t k = 0; k < d; ++k)
+            for (int64_t j = 0; j < fs; ++j)
+                W1i[k * fs + j] = W1[k * f + i * fs + j];
+        orc_matmul(X, W1i, Hi, M, d, fs);
+        orc_gelu_inplace(Hi, M * fs);
+        orc_matmul(Hi, W2 + i * fs * d, P + i * M * d, M, fs, d);
+    }
+    orc_reduce_scatter_rows(P, Ys, n_shards, M, d);
+    free(X); free(W1i); free(Hi); free(P);
+}

@@ -20,6 +20,13 @@ using namespace tpk;
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kInt32Max = 0x7FFFFFFF;
+// Largest element count of one matrix (2^40: 2 TiB of bf16, far above any
+// device's memory).  With it every byte count below (elements x at most 4
+// bytes x at most TP_MAX_SHARDS) stays far inside int64 / size_t.
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+// a * b <= kMaxElems for non-negative a, b, without forming the product.
+bool elems_ok(int64_t a, int64_t b) { return a == 0 || b <= kMaxElems / a; }
 
 // ----------------------------------------------------------------- devices --
 
@@ -388,7 +395,9 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.bn = plan.bn;
     a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
     a.n_tiles = static_cast<int>((c.N + a.bn - 1) / a.bn);
-    a.num_units = a.m_tiles * a.n_tiles * c.k_groups;
+    const int64_t units = static_cast<int64_t>(a.m_tiles) * a.n_tiles * c.k_groups;
+    if (units > kInt32Max) return TP_ERR_SHAPE;
+    a.num_units = static_cast<int>(units);
     a.out = c.out;
     a.out_group_stride = c.out_group_stride;
     a.out_f32 = c.out_f32 ? 1 : 0;
@@ -484,6 +493,12 @@ int reduce_grid(int64_t work_items, int sm_count) {
     return static_cast<int>(blocks);
 }
 
+// Largest single bulk copy of the reduce's producer.
+uint32_t red_piece_bytes(int n) {
+    (void)n;
+    return RED_STAGE_BYTES;
+}
+
 template <bool BF16>
 tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_count,
                           const void *bias, int64_t cols, cudaStream_t s) {
@@ -502,8 +517,9 @@ tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        const uint32_t piece = red_piece_bytes(n);
         if (cudaLaunchKernelEx(&cfg, shard_reduce_bulk_kernel<BF16>, P, Y, total, n, chunk,
-                               wait_limit_ns(), b, cols) != cudaSuccess)
+                               piece, wait_limit_ns(), b, cols) != cudaSuccess)
             return TP_ERR_CUDA;
         return launch_status();
     }
@@ -532,6 +548,7 @@ tp_status check_shards(int n_shards) {
 tp_status check_sizes(int64_t M, int64_t K, int64_t N) {
     if (M < 0 || K < 0 || N < 0) return TP_ERR_SHAPE;
     if (M > kInt32Max || K > kInt32Max || N > kInt32Max) return TP_ERR_SHAPE;
+    if (!elems_ok(M, K) || !elems_ok(K, N) || !elems_ok(M, N)) return TP_ERR_SHAPE;
     return TP_OK;
 }
 
@@ -898,7 +915,7 @@ tp_status tp_sharded_linear(const void *X, const void *W, void *Y, int64_t M, in
 
 tp_status tp_shard_reduce(const float *P, void *Y, int64_t rows, int64_t cols, int n_shards,
                           tp_dtype out_t, cudaStream_t s) {
-    if (rows < 0 || cols < 0) return TP_ERR_SHAPE;
+    if (rows < 0 || cols < 0 || !elems_ok(rows, cols)) return TP_ERR_SHAPE;
     if (!valid_dtype(out_t)) return TP_ERR_DTYPE;
     const int64_t total = rows * cols;
     if (!present(P, total) || !present(Y, total)) return TP_ERR_NULL;
@@ -913,7 +930,7 @@ tp_status tp_shard_reduce(const float *P, void *Y, int64_t rows, int64_t cols, i
 
 tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t shard_cols,
                                   int n_shards, int col_groups, tp_dtype t, cudaStream_t s) {
-    if (rows < 0 || shard_cols < 0) return TP_ERR_SHAPE;
+    if (rows < 0 || shard_cols < 0 || !elems_ok(rows, shard_cols)) return TP_ERR_SHAPE;
     if (!present(Ys, rows * shard_cols) || !present(Y, rows * shard_cols)) return TP_ERR_NULL;
     if (!valid_dtype(t)) return TP_ERR_DTYPE;
     tp_status st = check_shards(n_shards);
@@ -977,6 +994,9 @@ tp_status tp_qkv_linear(const void *X, const void *W, void *Y, void *Y_shards, i
                         int64_t K, int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim,
                         int n_shards, tp_dtype in_t, tp_dtype out_t, cudaStream_t s) {
     if (n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return TP_ERR_SHAPE;
+    if (n_q_heads > kInt32Max || n_kv_heads > kInt32Max ||
+        n_q_heads + 2 * n_kv_heads > kInt32Max / head_dim)
+        return TP_ERR_SHAPE;  // the projection's width must fit the GEMM's int sizes
     if (n_q_heads % n_kv_heads != 0) return TP_ERR_SHAPE;
     tp_status st = check_shards(n_shards);
     if (st != TP_OK) return st;
@@ -1037,7 +1057,8 @@ tp_status tp_shard_concat(const void *Ys, void *Y, int64_t rows, int64_t shard_c
 }
 
 size_t tp_mlp_block_workspace_size(int64_t M, int64_t f, tp_dtype t) {
-    if (M < 0 || f < 0 || !valid_dtype(t)) return 0;
+    if (M < 0 || f < 0 || M > kInt32Max || f > kInt32Max || !elems_ok(M, f) || !valid_dtype(t))
+        return 0;
     const size_t b = static_cast<size_t>(M) * static_cast<size_t>(f) * dtype_size(t);
     return (b + 255) & ~static_cast<size_t>(255);
 }
@@ -1079,7 +1100,8 @@ tp_status tp_row_linear_backward(const void *X, const void *W, const void *dY, v
 }
 
 size_t tp_mlp_block_backward_workspace_size(int64_t M, int64_t f, tp_dtype t) {
-    if (M < 0 || f < 0 || t != TP_BF16) return 0;
+    if (M < 0 || f < 0 || M > kInt32Max || f > kInt32Max || !elems_ok(M, f) || t != TP_BF16)
+        return 0;
     return 3 * ((static_cast<size_t>(M) * static_cast<size_t>(f) * 2 + 255) &
                 ~static_cast<size_t>(255));
 }

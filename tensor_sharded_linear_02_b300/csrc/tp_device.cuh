@@ -421,9 +421,11 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta_
 // Numerics shared by the epilogues.
 // ---------------------------------------------------------------------------
 // Exact (erf-form) GeLU, x * Phi(x) with Phi(x) = (1 + erf(x / sqrt 2)) / 2,
-// in fp32.  erf is evaluated with the rational approximation of Abramowitz
-// and Stegun, "Handbook of Mathematical Functions" (1964), formula 7.1.28:
-// for z >= 0,
+// in fp32, in two parts.
+//
+// Main part (x >= -3, and every x of a 32-value chunk with none below -3):
+// erf from the rational approximation of Abramowitz and Stegun, "Handbook of
+// Mathematical Functions" (1964), formula 7.1.28: for z >= 0,
 //     erfc(z) = 1 - erf(z) ~ (1 + a1 z + a2 z^2 + ... + a6 z^6)^-16,
 // absolute error at most 3e-7.  With z = |x| / sqrt 2 and h = erfc(z) / 2,
 // Phi(x) = 1 - h for x >= 0 and h for x < 0, so
@@ -434,12 +436,19 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta_
 // h = 1 / P^16.  Cost per element: 6 fused multiply-adds, 4 squarings, one
 // hardware reciprocal, a max and a fused multiply-add; the packed variant
 // does two elements per fp32x2 instruction (fma.rn.f32x2 / mul.rn.f32x2,
-// each lane rounded exactly like the scalar fmaf / multiply, so both give
-// identical results).  The error stays below 1e-6 max(1, |x|) (the
-// approximation, the rounding of the 16th power and of the reciprocal),
-// three orders of magnitude below the half-ulp (2^-9 relative) of the bf16
-// value the epilogue stores.  For |x| above ~28 the 16th power overflows to
-// +inf and h = 0, the correct limit.
+// each lane rounded exactly like the scalar fmaf / multiply).
+// The bound 3e-7 is absolute: relative to GeLU(x) = x h for x < 0 it grows
+// as h shrinks.  Evaluated in double, the relative error of this form is at
+// most 6.4e-5 over x >= -3 (largest near x = -2.97; below 1e-6 for x > 0),
+// 3.7e-3 at x = -4 and 4.7e-2 at x = -5.
+//
+// Tail (x < -3): GeLU(x) = x * Phi(x) with CUDA's normcdff, whose error is a
+// few ulp relative over its whole range, so the tail is as accurate
+// relatively as the rest.  It is a branch taken only for chunks that hold
+// such a value (for N(0, 1) pre-activations 1.35e-3 of the values).
+//
+// For |x| above ~28 the 16th power overflows to +inf and h = 0, the correct
+// limit on the positive side.
 constexpr float GELU_D0 = 1.04427373409271240e+00f;
 constexpr float GELU_D1 = -5.20751625299453735e-02f;
 constexpr float GELU_D2 = 2.20769979059696198e-02f;
@@ -447,8 +456,20 @@ constexpr float GELU_D3 = -3.42273921705782413e-03f;
 constexpr float GELU_D4 = 3.96861360059119761e-05f;
 constexpr float GELU_D5 = -5.10552090418059379e-05f;
 constexpr float GELU_D6 = 5.62129980608006008e-06f;
+constexpr float GELU_TAIL_X = -3.0f;
+// x < -3 (or a negative NaN) exactly when the fp32 bit pattern, read as an
+// unsigned integer, exceeds that of -3.0f (0xC0400000): positive values
+// have the sign bit clear, and among negative values a larger magnitude has
+// a larger pattern.
+constexpr uint32_t GELU_TAIL_BITS = 0xC0400000u;
 
-__device__ __forceinline__ float gelu_f32(float x) {
+// Inlined at every use: an out-of-line call would make the epilogues save
+// their live accumulator registers around it (measured: stack spills in the
+// cluster kernel), and the branch that reaches it is rarely taken.
+__device__ __forceinline__ float normcdf_tail_f32(float x) { return normcdff(x); }
+__device__ __forceinline__ float gelu_tail_f32(float x) { return x * normcdf_tail_f32(x); }
+
+__device__ __forceinline__ float gelu_main_f32(float x) {
     const float u = -fabsf(x);
     float p = fmaf(GELU_D6, u, GELU_D5);
     p = fmaf(p, u, GELU_D4);
@@ -463,6 +484,10 @@ __device__ __forceinline__ float gelu_f32(float x) {
     float h;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
     return fmaf(u, h, fmaxf(x, 0.0f));
+}
+
+__device__ __forceinline__ float gelu_f32(float x) {
+    return x < GELU_TAIL_X ? gelu_tail_f32(x) : gelu_main_f32(x);
 }
 
 // Two fp32 values in one 64-bit register (lo in bits 0-31) and the packed
@@ -486,8 +511,8 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// gelu_f32 of two values at once (same operations, same results).
-__device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
+// gelu_main_f32 of two values at once (same operations, same results).
+__device__ __forceinline__ void gelu2_main_f32(float &x0, float &x1) {
     const uint64_t u = f32x2_pack(-fabsf(x0), -fabsf(x1));
     uint64_t p = fma_f32x2(f32x2_pack(GELU_D6, GELU_D6), u, f32x2_pack(GELU_D5, GELU_D5));
     p = fma_f32x2(p, u, f32x2_pack(GELU_D4, GELU_D4));
@@ -508,21 +533,49 @@ __device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
     f32x2_unpack(y, x0, x1);
 }
 
-// GeLU of 32 values held as fp32 bit patterns (one tensor-memory load).
+// gelu_f32 of two values at once.
+__device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
+    const float a = x0, b = x1;
+    gelu2_main_f32(x0, x1);
+    if (fminf(a, b) < GELU_TAIL_X) {
+        if (a < GELU_TAIL_X) x0 = gelu_tail_f32(a);
+        if (b < GELU_TAIL_X) x1 = gelu_tail_f32(b);
+    }
+}
+
+// GeLU of 32 values held as fp32 bit patterns (one tensor-memory load).  The
+// common case (no value below -3: one unsigned maximum over the patterns)
+// runs the packed main part only; otherwise the values are taken pair by
+// pair with the tail check.
 __device__ __forceinline__ void gelu_chunk32(uint32_t (&r)[32]) {
+    uint32_t mx = r[0];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
-        gelu2_f32(a, b);
-        r[2 * i] = __float_as_uint(a);
-        r[2 * i + 1] = __float_as_uint(b);
+    for (int i = 1; i < 32; ++i) mx = max(mx, r[i]);
+    if (mx <= GELU_TAIL_BITS) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+            gelu2_main_f32(a, b);
+            r[2 * i] = __float_as_uint(a);
+            r[2 * i + 1] = __float_as_uint(b);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+            gelu2_f32(a, b);
+            r[2 * i] = __float_as_uint(a);
+            r[2 * i + 1] = __float_as_uint(b);
+        }
     }
 }
 
 // GeLU'(x) = Phi(x) + x * phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi), in fp32:
 // Phi from the same folded Abramowitz & Stegun 7.1.28 polynomial as
-// gelu_f32 (Phi = 1 - h for x >= 0, h for x < 0), the density from the
-// hardware base-2 exponential (exp(-x^2/2) = 2^(-x^2/2 * log2 e)).
+// gelu_main_f32 (Phi = 1 - h for x >= 0, h for x < 0) and, for x < -3, from
+// CUDA's normcdff (relative accuracy in the tail, as for the GeLU itself);
+// the density from the hardware base-2 exponential
+// (exp(-x^2/2) = 2^(-x^2/2 * log2 e)).
 __device__ __forceinline__ float gelu_grad_f32(float x) {
     const float u = -fabsf(x);
     float p = fmaf(GELU_D6, u, GELU_D5);
@@ -537,7 +590,8 @@ __device__ __forceinline__ float gelu_grad_f32(float x) {
     p = __fmul_rn(p, p);
     float h;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
-    const float phi_cdf = x >= 0.0f ? 1.0f - h : h;
+    float phi_cdf = x >= 0.0f ? 1.0f - h : h;
+    if (x < GELU_TAIL_X) phi_cdf = normcdf_tail_f32(x);
     float e;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * -0.72134752044448170368f));
     return fmaf(x * 0.39894228040143267794f, e, phi_cdf);

@@ -5,11 +5,12 @@ Accuracy bar (bf16 inputs, fp32 accumulation, compared with the fp64
 oracle on the same input bytes):
     relative Frobenius error  ||got - ref||_F / ||ref||_F  <= 5e-3
     elementwise |got - ref|  <= 2e-2 * RMS(ref) + u * |ref|
-where u is the unit roundoff of the output format: 2^-9 for a bf16 output,
+where u is the unit roundoff of the output format: 2^-8 for a bf16 output
+(8 significant bits: half the spacing of bf16 values in [1, 2) is 2^-8),
 0 for an fp32 output.  The 2e-2 * RMS term bounds the accumulated error of
 the fp32 result; a bf16 output then rounds each element to nearest, which
-by itself can move it by half an ulp (up to 2^-9 |y|) -- more than
-2e-2 * RMS whenever |y| exceeds about 10 RMS, as in the positive tail of a
+by itself can move it by half an ulp (up to 2^-8 |y|) -- more than
+2e-2 * RMS whenever |y| exceeds about 5 RMS, as in the positive tail of a
 GeLU output.  Tests that have both outputs also check that the bf16 output
 is exactly the round-to-nearest-even of the fp32 one.
 Integer-valued fp32 inputs must match exactly.
@@ -63,7 +64,7 @@ def errors(got, ref):
     return rel, mx, rms
 
 
-BF16_UNIT_ROUNDOFF = 2.0 ** -9
+BF16_UNIT_ROUNDOFF = 2.0 ** -8
 
 
 def assert_bf16_parity(got, ref, what="", out_bf16=True):

@@ -153,3 +153,92 @@ def test_binding_refuses_host_tensors():
     Y = torch.zeros(4, 16, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         binding.tp_column_linear(X, W, Y, None, n_shards=2)
+
+
+def test_binding_checks_every_shape_before_the_call():
+    """The C ABI sees bare pointers, so an output or second operand smaller
+    than the call's sizes imply would be read or written past its end: the
+    binding compares every tensor's shape and dtype with the sizes it
+    derives from X and W (or W1) and raises before any call.  (CPU tensors:
+    the shape checks come first, the device check last.)"""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    X = torch.zeros(4, 8, dtype=bf)
+    W = torch.zeros(8, 16, dtype=bf)
+    cases = [
+        (lambda: binding.tp_column_linear(X, W, torch.zeros(4, 15, dtype=bf), n_shards=2), "Y"),
+        (lambda: binding.tp_column_linear(X, torch.zeros(7, 16, dtype=bf), None,
+                                          torch.zeros(2, 4, 8, dtype=bf), n_shards=2), "rows"),
+        (lambda: binding.tp_column_linear(X, W, None, torch.zeros(2, 4, 7, dtype=bf),
+                                          n_shards=2), "Y_shards"),
+        (lambda: binding.tp_column_linear(X, W.float(), torch.zeros(4, 16, dtype=bf)), "dtype"),
+        (lambda: binding.tp_column_linear(X, W, torch.zeros(4, 16, dtype=bf),
+                                          torch.zeros(2, 4, 8, dtype=f32), n_shards=2), "dtype"),
+        (lambda: binding.tp_column_linear_bias(X, W, torch.zeros(15, dtype=bf),
+                                               torch.zeros(4, 16, dtype=bf)), "bias"),
+        (lambda: binding.tp_row_linear(X, W, torch.zeros(4, 16, dtype=bf),
+                                       torch.zeros(2, 4, 16, dtype=bf), n_shards=2), "P_out"),
+        (lambda: binding.tp_row_linear(X, W, None, torch.zeros(3, 4, 16, dtype=f32),
+                                       n_shards=2), "P_out"),
+        (lambda: binding.tp_shard_reduce(torch.zeros(2, 4, 16, dtype=f32),
+                                         torch.zeros(4, 8, dtype=bf)), "Y"),
+        (lambda: binding.tp_shard_reduce(torch.zeros(2, 4, 16, dtype=bf),
+                                         torch.zeros(4, 16, dtype=bf)), "P"),
+        (lambda: binding.tp_shard_concat(torch.zeros(2, 4, 8, dtype=bf),
+                                         torch.zeros(4, 15, dtype=bf)), "Y"),
+        (lambda: binding.tp_shard_concat_grouped(torch.zeros(2, 4, 8, dtype=bf),
+                                                 torch.zeros(4, 16, dtype=f32)), "dtype"),
+        (lambda: binding.tp_mlp_block(X, W, torch.zeros(16, 7, dtype=bf),
+                                      torch.zeros(4, 8, dtype=bf), torch.zeros(256, dtype=torch.uint8)),
+         "W2"),
+        (lambda: binding.tp_mlp_block(X, W, torch.zeros(16, 8, dtype=bf),
+                                      torch.zeros(5, 8, dtype=bf), torch.zeros(256, dtype=torch.uint8)),
+         "Y"),
+        (lambda: binding.tp_mlp_block(X, W, torch.zeros(16, 8, dtype=f32),
+                                      torch.zeros(4, 8, dtype=bf), torch.zeros(256, dtype=torch.uint8)),
+         "dtype"),
+        (lambda: binding.tp_mlp_block_bias(X, W, torch.zeros(8, dtype=bf), torch.zeros(16, 8, dtype=bf),
+                                           None, torch.zeros(4, 8, dtype=bf),
+                                           torch.zeros(256, dtype=torch.uint8)), "b1"),
+        (lambda: binding.tp_mlp_block_static_ws(X, W, torch.zeros(16, 8, dtype=bf),
+                                                torch.zeros(4, 9, dtype=bf)), "Y"),
+        (lambda: binding.tp_qkv_linear(X, torch.zeros(8, 6 * 4, dtype=bf),
+                                       torch.zeros(4, 6 * 4, dtype=bf), None, n_q_heads=4,
+                                       n_kv_heads=2, head_dim=4), "W"),
+        (lambda: binding.tp_qkv_linear(X, torch.zeros(8, 8 * 4, dtype=bf),
+                                       torch.zeros(4, 8 * 4, dtype=bf),
+                                       torch.zeros(2, 4, 12, dtype=bf), n_q_heads=4,
+                                       n_kv_heads=2, head_dim=4, n_shards=2), "Y_shards"),
+        (lambda: binding.tp_column_linear_backward(X, W, torch.zeros(4, 16, dtype=bf),
+                                                   torch.zeros(4, 7, dtype=bf)), "dX"),
+        (lambda: binding.tp_row_linear_backward(X, W, torch.zeros(3, 16, dtype=bf)), "dY"),
+        (lambda: binding.tp_mlp_block_backward(X, W, torch.zeros(16, 8, dtype=bf),
+                                               torch.zeros(4, 8, dtype=bf),
+                                               torch.zeros(256, dtype=torch.uint8),
+                                               dW2=torch.zeros(8, 16, dtype=bf)), "dW2"),
+        (lambda: binding.tp_column_linear(torch.zeros(4, 8, 1, dtype=bf), W, None), "dimensions"),
+    ]
+    for fn, what in cases:
+        with pytest.raises(ValueError, match=what):
+            fn()
+    # a consistent call gets past the shape checks and stops at the device check
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.tp_row_linear(X, W, torch.zeros(4, 16, dtype=bf),
+                              torch.zeros(2, 4, 16, dtype=f32), n_shards=2)
+
+
+def test_absurd_sizes_are_refused_without_overflow(lib):
+    """Sizes whose products would overflow 64-bit byte counts (or exceed any
+    device's memory) are refused with TP_ERR_SHAPE before anything else."""
+    big = (1 << 31) - 1
+    assert _col(lib, M=big, K=big, N=64) == SHAPE
+    assert _col(lib, M=16, K=big, N=big - 7) == SHAPE
+    assert _row(lib, M=big, K=32, N=big - 7) == SHAPE
+    assert lib.tp_shard_reduce(A, C, 1 << 40, 1 << 30, 2, BF16, None) == SHAPE
+    assert lib.tp_shard_concat(A, C, 1 << 40, 1 << 30, 2, BF16, None) == SHAPE
+    assert lib.tp_qkv_linear(A, B, C, None, 16, 32, big, big, big, 1, BF16, BF16, None) == SHAPE
+    assert lib.tp_mlp_block_workspace_size(1 << 33, 1 << 31, BF16) == 0
+    assert lib.tp_mlp_block_workspace_size(big, big, BF16) == 0
+    assert lib.tp_mlp_block_backward_workspace_size(big, big, BF16) == 0
+    assert lib.tp_mlp_block(A, B, C, D, 0x50000000, 1 << 20, big, big, 8, 2, BF16, BF16,
+                            None) == SHAPE

@@ -177,3 +177,58 @@ def test_backward_validation(tp, cuda_device):
         tp.tp_column_linear_backward(X.float(), W.float(), dY.float(), dX.float(), None)
     assert e.value.status == 5
     assert tp.tp_get_device_status() == tp.TP_OK
+
+
+def test_gelu_grad_epilogue_accuracy(tp, cuda_device):
+    """The backward epilogue's GeLU'(z) = Phi(z) + z phi(z) at every bf16 z in
+    [-12, 12], isolated: with W1 = [I_8 | I_8 | ...] the recomputed
+    pre-activation Z = X.W1 copies X's entries exactly, and with dY = e_0 and
+    W2[:, 0] = 1 the product dY.W2^T is 1 everywhere, so the dZ stored in the
+    workspace is bf16(GeLU'(z)).  Bound: one bf16 ulp of the round-to-
+    nearest-even of the fp64 value, except near the zero of GeLU' (where
+    the two terms cancel and only an error relative to their magnitude,
+    Phi(z) + |z| phi(z), is meaningful: 2^-8 of the value plus 1e-4 of that
+    magnitude), and nothing below 1e-30."""
+    import math
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_to_f64(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 12.0)
+    xb, xs = bits[keep], vals[keep]
+    pad = (-xb.size) % 8
+    xb = np.concatenate([xb, np.zeros(pad, np.uint16)])
+    xs = np.concatenate([xs, np.zeros(pad)])
+    M, d, f = xb.size // 8, 8, 8 * 33
+    w1 = np.zeros((d, f))
+    w1[np.arange(f) % 8, np.arange(f)] = 1.0
+    w2 = np.zeros((f, d))
+    w2[:, 0] = 1.0
+    g = np.zeros((M, d))
+    g[:, 0] = 1.0
+    X = to_dev_bf16(xb.reshape(M, d), cuda_device)
+    W1, W2, dY = (to_dev_bf16(oracle.f64_to_bf16(a), cuda_device) for a in (w1, w2, g))
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=cuda_device)
+    dX = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, None, None, n_shards=1)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    part = (M * f * 2 + 255) // 256 * 256
+    dZ = ws[2 * part: 2 * part + M * f * 2].view(torch.int16).view(M, f)
+    got_bits = dZ.cpu().numpy().view(np.uint16)
+    z = xs.reshape(M, d)[:, np.arange(f) % 8]
+    ref = oracle.gelu_grad(z.ravel()).reshape(M, f)
+    got = oracle.bf16_to_f64(got_bits)
+    phi = np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+    scale = 0.5 * (1.0 + np.vectorize(math.erf)(z / math.sqrt(2.0))) + np.abs(z) * phi
+    want = oracle.f64_to_bf16(ref)
+    line = lambda b: np.where(b.astype(np.int64) & 0x8000, -(b.astype(np.int64) & 0x7FFF),
+                              b.astype(np.int64) & 0x7FFF)
+    ulps = np.abs(line(got_bits) - line(want))
+    ok = ((ulps <= 1) | (np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-4 * scale)
+          | (np.abs(ref) < 1e-30) & (np.abs(got) < 1e-30))
+    worst = int(np.argmin(ok))
+    assert ok.all(), (f"GeLU'({z.flat[worst]!r}) -> {got.flat[worst]!r}, oracle "
+                      f"{ref.flat[worst]!r} ({ulps.flat[worst]} ulp)")
+    # where the terms do not cancel, the one-ulp bound holds on its own
+    clear = np.abs(ref) >= 0.05 * scale
+    assert np.all(ulps[clear & (np.abs(ref) >= 1e-30)] <= 1)

@@ -153,6 +153,99 @@ def test_mlp_brute_force_with_library_gelu():
         np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
 
 
+def _bf16_round_py(v):
+    """Round a double to the nearest bf16 value, ties to even, by exact
+    float arithmetic: frexp gives v = m 2^e with 0.5 <= |m| < 1, m * 2^8 is
+    exact, and Python's round() rounds halves to even (normal range only)."""
+    if v == 0.0:
+        return v
+    m, e = math.frexp(v)
+    return math.ldexp(round(m * 256.0), e - 8)
+
+
+def test_mlp_mirror_mode_rounds_hidden_to_bf16():
+    """The oracle's diagnostic mode (hidden activation rounded to bf16 before
+    the second product) against plain loops: GeLU from scipy's normal CDF,
+    each H value rounded to bf16 by _bf16_round_py, then the row product
+    and the ascending shard sum.  The mode must also differ from the plain
+    oracle (the rounding really happens), by no more than the rounding of H
+    allows."""
+    rng = np.random.default_rng(11)
+    for M, d, f, n in [(3, 4, 8, 2), (2, 5, 6, 3), (4, 8, 16, 4), (1, 2, 2, 1)]:
+        X = rng.standard_normal((M, d))
+        W1 = rng.standard_normal((d, f))
+        W2 = rng.standard_normal((f, d))
+        H = [[sum(X[i, k] * W1[k, j] for k in range(d)) for j in range(f)] for i in range(M)]
+        H = [[_bf16_round_py(h * float(scipy.special.ndtr(h))) for h in row] for row in H]
+        fs = f // n
+        Y = [[sum(sum(H[i][s * fs + k] * W2[s * fs + k, j] for k in range(fs)) for s in range(n))
+              for j in range(d)] for i in range(M)]
+        got = oracle.mlp_block(X, W1, W2, n, mirror_h_bf16=True)
+        np.testing.assert_allclose(got, Y, rtol=1e-12, atol=1e-12)
+        plain = oracle.mlp_block(X, W1, W2, n)
+        assert not np.array_equal(got, plain)
+        # |H_bf16 - H| <= 2^-8 |H| (8 significant bits), so
+        # |dY| <= 2^-8 sum_k |H_k| |W2_kj|
+        Hp = np.array([[h * scipy.special.ndtr(h) for h in row] for row in (X @ W1)])
+        bound = 2.0 ** -8 * (np.abs(Hp) @ np.abs(W2)) + 1e-12
+        assert np.all(np.abs(got - plain) <= bound)
+
+
+def test_sequence_parallel_combines_brute_force():
+    """Sequence-parallel combines ([TP-topic] "Sequence Parallelism
+    Extension") on tiny integer shapes against plain Python: the all-gather
+    stacks the token blocks in shard order, and the combine after the block
+    gives shard i the sum over all shards' partials of its own token rows
+    [i*M/n, (i+1)*M/n).  Planted mistakes (own partial only, another
+    shard's rows, a dropped shard) are rejected."""
+    rnd = random.Random(5)
+    for n, Mb, cols in [(1, 3, 2), (2, 2, 3), (3, 1, 4), (4, 2, 1), (8, 1, 2)]:
+        M = n * Mb
+        P = [[[rnd.randint(-9, 9) for _ in range(cols)] for _ in range(M)] for _ in range(n)]
+        want = [[[sum(P[j][i * Mb + r][c] for j in range(n)) for c in range(cols)]
+                 for r in range(Mb)] for i in range(n)]
+        got = oracle.reduce_scatter_rows(np.array(P, dtype=np.float64))
+        np.testing.assert_array_equal(got, want)
+        own_only = [[P[i][i * Mb + r] for r in range(Mb)] for i in range(n)]
+        if n > 1:
+            assert not np.array_equal(got, own_only)
+            assert not np.array_equal(got, np.roll(np.array(want), 1, axis=0))
+            dropped = [[[sum(P[j][i * Mb + r][c] for j in range(n - 1)) for c in range(cols)]
+                        for r in range(Mb)] for i in range(n)]
+            assert not np.array_equal(got, dropped) or not any(
+                P[n - 1][r][c] for r in range(M) for c in range(cols))
+        Xs = [[[rnd.randint(-9, 9) for _ in range(cols)] for _ in range(Mb)] for _ in range(n)]
+        gathered = [row for block in Xs for row in block]
+        np.testing.assert_array_equal(oracle.allgather_rows(np.array(Xs, dtype=np.float64)),
+                                      gathered)
+
+
+def test_sequence_parallel_mlp_block_brute_force():
+    """The MLP block between two sequence-split regions: token blocks
+    all-gathered, each shard's GeLU(X.W1_i).W2_i for every token (GeLU from
+    scipy's normal CDF), partials summed and split by token rows; against
+    plain loops, for every shard count dividing both the tokens and f."""
+    rng = np.random.default_rng(9)
+    for n, Mb, d, f in [(1, 3, 4, 4), (2, 2, 3, 4), (3, 1, 2, 6), (4, 2, 2, 8)]:
+        M = n * Mb
+        Xs = rng.standard_normal((n, Mb, d))
+        W1 = rng.standard_normal((d, f))
+        W2 = rng.standard_normal((f, d))
+        X = [list(Xs[i, r]) for i in range(n) for r in range(Mb)]
+        fs = f // n
+        P = []
+        for s_ in range(n):
+            H = [[sum(X[t][k] * W1[k, s_ * fs + j] for k in range(d)) for j in range(fs)]
+                 for t in range(M)]
+            H = [[h * float(scipy.special.ndtr(h)) for h in row] for row in H]
+            P.append([[sum(H[t][j] * W2[s_ * fs + j, c] for j in range(fs)) for c in range(d)]
+                      for t in range(M)])
+        want = [[[sum(P[s_][i * Mb + r][c] for s_ in range(n)) for c in range(d)]
+                 for r in range(Mb)] for i in range(n)]
+        got = oracle.seq_parallel_mlp_block(Xs, W1, W2)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
 def test_bias_brute_force_integer_shapes():
     """Biases on tiny integer shapes against plain Python loops: the column
     split adds each shard's slice of the bias to its outputs, the row split

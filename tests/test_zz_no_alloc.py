@@ -4,7 +4,10 @@ cudaMalloc once running, or a host that owns all device memory in its own
 pool and passes the library only inputs and outputs).  Its scratch is a
 fixed array inside the library, so it is checked here against the
 caller-workspace entry point, on two calls in a row: the second call must
-not be affected by what the first one left in the shared array.
+not be affected by what the first one left in the shared array.  Both entry
+points run the same kernels in the same order on the same inputs, so their
+outputs must agree bit for bit (and, like every MLP-block result, sit
+within the accuracy bar of each other).
 
 This file is collected last on purpose: if it fails, a run that stops at
 the first failure has already run every other test.
@@ -12,7 +15,7 @@ the first failure has already run every other test.
 import numpy as np
 import pytest
 
-from helpers import assert_bf16_parity, bf16_dev_to_f64, to_dev_bf16
+from helpers import assert_bf16_parity, bf16_dev_to_f64, dev_bits, to_dev_bf16
 from tensor_sharded_linear_02_b300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -31,6 +34,7 @@ def _case(tp, dev, M, d, f, n, seed):
     Y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=dev)
     tp.tp_mlp_block_static_ws(X, W1, W2, Y, n_shards=n)
     assert tp.tp_get_device_status() == tp.TP_OK
+    np.testing.assert_array_equal(dev_bits(Y), dev_bits(Y_ref))
     return bf16_dev_to_f64(Y), bf16_dev_to_f64(Y_ref)
 
 
