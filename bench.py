@@ -265,7 +265,7 @@ def _kernel_split(tp, torch, X, W1, W2, H, Y, n, flush, stream, K):
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     for i in range(K):
         _prequeue(torch, i)
-        flush.zero_()
+        _flush_l2(flush)
         ev3[i][0].record(stream)
         tp.tp_column_linear(X, W1, H, None, n_shards=n, act="gelu")
         ev3[i][1].record(stream)
@@ -356,7 +356,7 @@ def run_ours(args):
         tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        _flush_l2(flush)
         step()
     torch.cuda.synchronize()
     if tp.tp_get_device_status() != tp.TP_OK:
@@ -377,7 +377,7 @@ def run_ours(args):
         t_wall0 = time.perf_counter()
         for i in range(K):
             _prequeue(torch, i)
-            flush.zero_()
+            _flush_l2(flush)
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -447,7 +447,7 @@ def run_ours(args):
         "data": "synthetic (seeded SplitMix64/Box-Muller, bf16)",
         "config": {"workload": args.workload, "M": M, "d": d, "f": f, "n_shards": n,
                    "weight_std": std, "flops_per_step": flops_step,
-                   "l2": "flushed before every timed step (256 MB write)",
+                   "l2": "flushed before every timed step (256 MB write, then read)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "frac_of_peak": round(value / peak, 4),
         "roofline": roofline,
@@ -495,11 +495,24 @@ def bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=2000):
     return {"workload": name, "value": round(tf, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
             "steps": K, "roofline": _gemm_roofline(name, k1_ms, k2_ms, flops, flops, peaks),
-            "l2": "flushed before every timed step (256 MB write)"}
+            "l2": "flushed before every timed step (256 MB write, then read)"}
 
 
 PREQUEUE_BATCH = 20
 PREQUEUE_SLEEP_CYCLES = 10_000_000  # ~5 ms at 2 GHz, longer than enqueuing a batch
+
+
+def _flush_l2(buf):
+    """Evicts the step's data from L2 between timed iterations: a write of a
+    buffer twice the size of L2 (126 MB), then a read of the same buffer.
+    The read makes the write-back of the dirty lines the write leaves in L2
+    happen here, outside the timed interval, so that the timed kernel starts
+    with a cold L2 holding no dirty lines (otherwise up to 126 MB of write-
+    back land inside the timed interval, a large error for the HBM-bound
+    kernels: measured 4.9 vs 6.5 TB/s for the one-shard reduce)."""
+    import torch
+    buf.zero_()
+    buf.view(torch.int32).sum()
 
 
 def _prequeue(torch, i):
@@ -694,7 +707,7 @@ def _time_steps(torch, step, flush, stream, K):
     torch.cuda.synchronize()
     for i in range(K):
         _prequeue(torch, i)
-        flush.zero_()
+        _flush_l2(flush)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -786,7 +799,7 @@ def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
           for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()
+        _flush_l2(flush)
         ev[i][0].record(stream)
         tp.tp_shard_reduce(P, Y)
         ev[i][1].record(stream)
@@ -800,7 +813,7 @@ def bench_reduce(tp, dev, stream, peaks, K=200, n=8, rows=4096, cols=8192):
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": _profile_traffic(f"reduce_{n}x{rows}x{cols}"),
                          "peak_source": peaks["source"] + " copy bandwidth"},
-            "l2": "flushed before every timed launch (256 MB write)"}
+            "l2": "flushed before every timed launch (256 MB write, then read)"}
 
 
 def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=3):
@@ -814,7 +827,7 @@ def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=
           for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()
+        _flush_l2(flush)
         ev[i][0].record(stream)
         tp.tp_shard_concat_grouped(Ys, Y, col_groups=groups)
         ev[i][1].record(stream)
@@ -829,7 +842,7 @@ def bench_concat(tp, dev, stream, peaks, K=200, n=8, rows=8192, sc=1536, groups=
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": _profile_traffic(f"concat_{n}x{rows}x{sc}_g{groups}"),
                          "peak_source": peaks["source"] + " copy bandwidth"},
-            "l2": "flushed before every timed launch"}
+            "l2": "flushed before every timed launch (256 MB write, then read)"}
 
 
 def run_leg(args):

@@ -421,77 +421,78 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t cta_
 // Numerics shared by the epilogues.
 // ---------------------------------------------------------------------------
 // Exact (erf-form) GeLU, x * Phi(x) with Phi(x) = (1 + erf(x / sqrt 2)) / 2,
-// in fp32, in two parts.
+// in fp32, written as
+//     GeLU(x) = max(x, 0) - |x| h,   h = Phi(-|x|) = erfc(|x| / sqrt 2) / 2,
+// with h accurate RELATIVE to its value over the whole range: for x < 0,
+// GeLU(x) = x h shrinks like exp(-x^2 / 2), so an error bound that is only
+// absolute (as for the rational approximations of erf) says nothing there.
 //
-// Main part (x >= -3, and every x of a 32-value chunk with none below -3):
-// erf from the rational approximation of Abramowitz and Stegun, "Handbook of
-// Mathematical Functions" (1964), formula 7.1.28: for z >= 0,
-//     erfc(z) = 1 - erf(z) ~ (1 + a1 z + a2 z^2 + ... + a6 z^6)^-16,
-// absolute error at most 3e-7.  With z = |x| / sqrt 2 and h = erfc(z) / 2,
-// Phi(x) = 1 - h for x >= 0 and h for x < 0, so
-//     GeLU(x) = max(x, 0) - |x| h.
-// The constants are folded into the polynomial: with u = -|x| and
-// k = 2^(1/16), P(u) = sum_i d_i u^i, d_i = k a_i (-1/sqrt 2)^i (d_0 = k),
-// equals k (1 + a1 z + ... + a6 z^6), so P^16 = 2 / erfc(z) and
-// h = 1 / P^16.  Cost per element: 6 fused multiply-adds, 4 squarings, one
-// hardware reciprocal, a max and a fused multiply-add; the packed variant
-// does two elements per fp32x2 instruction (fma.rn.f32x2 / mul.rn.f32x2,
-// each lane rounded exactly like the scalar fmaf / multiply).
-// The bound 3e-7 is absolute: relative to GeLU(x) = x h for x < 0 it grows
-// as h shrinks.  Evaluated in double, the relative error of this form is at
-// most 6.4e-5 over x >= -3 (largest near x = -2.97; below 1e-6 for x > 0),
-// 3.7e-3 at x = -4 and 4.7e-2 at x = -5.
-//
-// Tail (x < -3): GeLU(x) = x * Phi(x) with CUDA's normcdff, whose error is a
-// few ulp relative over its whole range, so the tail is as accurate
-// relatively as the rest.  It is a branch taken only for chunks that hold
-// such a value (for N(0, 1) pre-activations 1.35e-3 of the values).
-//
-// For |x| above ~28 the 16th power overflows to +inf and h = 0, the correct
-// limit on the positive side.
-constexpr float GELU_D0 = 1.04427373409271240e+00f;
-constexpr float GELU_D1 = -5.20751625299453735e-02f;
-constexpr float GELU_D2 = 2.20769979059696198e-02f;
-constexpr float GELU_D3 = -3.42273921705782413e-03f;
-constexpr float GELU_D4 = 3.96861360059119761e-05f;
-constexpr float GELU_D5 = -5.10552090418059379e-05f;
-constexpr float GELU_D6 = 5.62129980608006008e-06f;
-constexpr float GELU_TAIL_X = -3.0f;
-// x < -3 (or a negative NaN) exactly when the fp32 bit pattern, read as an
-// unsigned integer, exceeds that of -3.0f (0xC0400000): positive values
-// have the sign bit clear, and among negative values a larger magnitude has
-// a larger pattern.
-constexpr uint32_t GELU_TAIL_BITS = 0xC0400000u;
+// h uses the functional form of the Chebyshev-fitted complementary error
+// function of Press, Teukolsky, Vetterling & Flannery, "Numerical Recipes
+// in C" (2nd ed.), section 6.2: erfc(z) = t exp(-z^2 + P(t)) with
+// t = 1 / (1 + z / 2), P a polynomial.  As z runs over [0, inf), t runs
+// over (0, 1] and ln(erfc(z) exp(z^2) / t) is smooth, so a polynomial of
+// degree 7 fits it; the coefficients below come from a least-squares
+// Chebyshev fit over t in [0.09, 1] (|x| up to 28; fit_gelu.py in the
+// package), folded for the base-2 exponential and the factor 1/2:
+//     t = 1 / (1 + |x| / (2 sqrt 2)),
+//     h = t * 2^(G(t) - x^2 log2(e) / 2),   G(t) = log2(e) (P(t) - ln 2).
+// Relative error of h in double: 7.4e-7.  In fp32 (one hardware reciprocal,
+// 8 fused multiply-adds, one hardware base-2 exponential, a multiply, a max
+// and a fused multiply-add, two elements per packed fma.rn.f32x2 /
+// mul.rn.f32x2 instruction where the operation allows) an emulation over
+// every bf16 input in [-12, 12] gives a GeLU relative error of at most
+// 6.5e-6 (the rounding of the exponent's argument, largest in the far
+// tail), and the bf16 rounding of every value equal to the round-to-
+// nearest-even of the exact GeLU.  Straight-line code: no branch, so no
+// code is replicated per element in the unrolled epilogues.  For |x| past
+// ~13 the exponential underflows to 0 (ftz) and GeLU(x) = max(x, 0), the
+// correct limit to fp32 precision.
+constexpr float GELU_T_SCALE = 3.535533906e-01f;  // 1 / (2 sqrt 2)
+constexpr float GELU_G0 = -2.825663090e+00f;
+constexpr float GELU_G1 = 1.440122604e+00f;
+constexpr float GELU_G2 = 5.716950893e-01f;
+constexpr float GELU_G3 = -6.818283349e-02f;
+constexpr float GELU_G4 = 5.251461267e-01f;
+constexpr float GELU_G5 = -1.465897799e+00f;
+constexpr float GELU_G6 = 1.096563697e+00f;
+constexpr float GELU_G7 = -2.737848759e-01f;
+constexpr float GELU_HALF_LOG2E = 7.213475204e-01f;  // log2(e) / 2
+constexpr float INV_SQRT_2PI = 3.989422804e-01f;
 
-// Inlined at every use: an out-of-line call would make the epilogues save
-// their live accumulator registers around it (measured: stack spills in the
-// cluster kernel), and the branch that reaches it is rarely taken.
-__device__ __forceinline__ float normcdf_tail_f32(float x) { return normcdff(x); }
-__device__ __forceinline__ float gelu_tail_f32(float x) { return x * normcdf_tail_f32(x); }
+__device__ __forceinline__ float rcp_approx(float a) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
 
-__device__ __forceinline__ float gelu_main_f32(float x) {
-    const float u = -fabsf(x);
-    float p = fmaf(GELU_D6, u, GELU_D5);
-    p = fmaf(p, u, GELU_D4);
-    p = fmaf(p, u, GELU_D3);
-    p = fmaf(p, u, GELU_D2);
-    p = fmaf(p, u, GELU_D1);
-    p = fmaf(p, u, GELU_D0);
-    p = __fmul_rn(p, p);  // ^2
-    p = __fmul_rn(p, p);  // ^4
-    p = __fmul_rn(p, p);  // ^8
-    p = __fmul_rn(p, p);  // ^16
-    float h;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
-    return fmaf(u, h, fmaxf(x, 0.0f));
+__device__ __forceinline__ float ex2_approx(float a) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+
+// h = Phi(-|x|), relative error ~1e-6 (see above).
+__device__ __forceinline__ float normal_tail_f32(float x) {
+    const float u = fabsf(x);
+    const float t = rcp_approx(fmaf(u, GELU_T_SCALE, 1.0f));
+    float g = fmaf(GELU_G7, t, GELU_G6);
+    g = fmaf(g, t, GELU_G5);
+    g = fmaf(g, t, GELU_G4);
+    g = fmaf(g, t, GELU_G3);
+    g = fmaf(g, t, GELU_G2);
+    g = fmaf(g, t, GELU_G1);
+    g = fmaf(g, t, GELU_G0);
+    return t * ex2_approx(fmaf(x * -GELU_HALF_LOG2E, x, g));
 }
 
 __device__ __forceinline__ float gelu_f32(float x) {
-    return x < GELU_TAIL_X ? gelu_tail_f32(x) : gelu_main_f32(x);
+    return fmaf(-fabsf(x), normal_tail_f32(x), fmaxf(x, 0.0f));
 }
 
 // Two fp32 values in one 64-bit register (lo in bits 0-31) and the packed
-// fp32x2 arithmetic of sm_100-class GPUs.
+// fp32x2 arithmetic of sm_100-class GPUs (each lane rounded exactly like the
+// scalar instruction, so packed and scalar evaluations agree bit for bit).
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -510,91 +511,52 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t splat2(float c) { return f32x2_pack(c, c); }
 
-// gelu_main_f32 of two values at once (same operations, same results).
-__device__ __forceinline__ void gelu2_main_f32(float &x0, float &x1) {
-    const uint64_t u = f32x2_pack(-fabsf(x0), -fabsf(x1));
-    uint64_t p = fma_f32x2(f32x2_pack(GELU_D6, GELU_D6), u, f32x2_pack(GELU_D5, GELU_D5));
-    p = fma_f32x2(p, u, f32x2_pack(GELU_D4, GELU_D4));
-    p = fma_f32x2(p, u, f32x2_pack(GELU_D3, GELU_D3));
-    p = fma_f32x2(p, u, f32x2_pack(GELU_D2, GELU_D2));
-    p = fma_f32x2(p, u, f32x2_pack(GELU_D1, GELU_D1));
-    p = fma_f32x2(p, u, f32x2_pack(GELU_D0, GELU_D0));
-    p = mul_f32x2(p, p);
-    p = mul_f32x2(p, p);
-    p = mul_f32x2(p, p);
-    p = mul_f32x2(p, p);
-    float q0, q1, h0, h1;
-    f32x2_unpack(p, q0, q1);
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(q0));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(q1));
-    const uint64_t y =
-        fma_f32x2(u, f32x2_pack(h0, h1), f32x2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)));
+// gelu_f32 of two values at once (same operations, same results).
+__device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
+    const uint64_t u = f32x2_pack(fabsf(x0), fabsf(x1));
+    const uint64_t den = fma_f32x2(u, splat2(GELU_T_SCALE), splat2(1.0f));
+    float d0, d1;
+    f32x2_unpack(den, d0, d1);
+    const uint64_t t = f32x2_pack(rcp_approx(d0), rcp_approx(d1));
+    uint64_t g = fma_f32x2(splat2(GELU_G7), t, splat2(GELU_G6));
+    g = fma_f32x2(g, t, splat2(GELU_G5));
+    g = fma_f32x2(g, t, splat2(GELU_G4));
+    g = fma_f32x2(g, t, splat2(GELU_G3));
+    g = fma_f32x2(g, t, splat2(GELU_G2));
+    g = fma_f32x2(g, t, splat2(GELU_G1));
+    g = fma_f32x2(g, t, splat2(GELU_G0));
+    const uint64_t xx = f32x2_pack(x0, x1);
+    const uint64_t a = fma_f32x2(mul_f32x2(xx, splat2(-GELU_HALF_LOG2E)), xx, g);
+    float a0, a1;
+    f32x2_unpack(a, a0, a1);
+    const uint64_t h = mul_f32x2(t, f32x2_pack(ex2_approx(a0), ex2_approx(a1)));
+    const uint64_t nu = f32x2_pack(-fabsf(x0), -fabsf(x1));
+    const uint64_t y = fma_f32x2(nu, h, f32x2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)));
     f32x2_unpack(y, x0, x1);
 }
 
-// gelu_f32 of two values at once.
-__device__ __forceinline__ void gelu2_f32(float &x0, float &x1) {
-    const float a = x0, b = x1;
-    gelu2_main_f32(x0, x1);
-    if (fminf(a, b) < GELU_TAIL_X) {
-        if (a < GELU_TAIL_X) x0 = gelu_tail_f32(a);
-        if (b < GELU_TAIL_X) x1 = gelu_tail_f32(b);
-    }
-}
-
-// GeLU of 32 values held as fp32 bit patterns (one tensor-memory load).  The
-// common case (no value below -3: one unsigned maximum over the patterns)
-// runs the packed main part only; otherwise the values are taken pair by
-// pair with the tail check.
+// GeLU of 32 values held as fp32 bit patterns (one tensor-memory load).
 __device__ __forceinline__ void gelu_chunk32(uint32_t (&r)[32]) {
-    uint32_t mx = r[0];
 #pragma unroll
-    for (int i = 1; i < 32; ++i) mx = max(mx, r[i]);
-    if (mx <= GELU_TAIL_BITS) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
-            gelu2_main_f32(a, b);
-            r[2 * i] = __float_as_uint(a);
-            r[2 * i + 1] = __float_as_uint(b);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
-            gelu2_f32(a, b);
-            r[2 * i] = __float_as_uint(a);
-            r[2 * i + 1] = __float_as_uint(b);
-        }
+    for (int i = 0; i < 16; ++i) {
+        float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+        gelu2_f32(a, b);
+        r[2 * i] = __float_as_uint(a);
+        r[2 * i + 1] = __float_as_uint(b);
     }
 }
 
-// GeLU'(x) = Phi(x) + x * phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi), in fp32:
-// Phi from the same folded Abramowitz & Stegun 7.1.28 polynomial as
-// gelu_main_f32 (Phi = 1 - h for x >= 0, h for x < 0) and, for x < -3, from
-// CUDA's normcdff (relative accuracy in the tail, as for the GeLU itself);
-// the density from the hardware base-2 exponential
-// (exp(-x^2/2) = 2^(-x^2/2 * log2 e)).
+// GeLU'(x) = Phi(x) + x phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi), in fp32:
+// Phi from the same normal tail as gelu_f32 (Phi = 1 - h for x >= 0, h for
+// x < 0, so relative accuracy holds in the negative tail too), the density
+// from the hardware base-2 exponential (exp(-x^2/2) = 2^(-x^2 log2(e) / 2)).
 __device__ __forceinline__ float gelu_grad_f32(float x) {
-    const float u = -fabsf(x);
-    float p = fmaf(GELU_D6, u, GELU_D5);
-    p = fmaf(p, u, GELU_D4);
-    p = fmaf(p, u, GELU_D3);
-    p = fmaf(p, u, GELU_D2);
-    p = fmaf(p, u, GELU_D1);
-    p = fmaf(p, u, GELU_D0);
-    p = __fmul_rn(p, p);
-    p = __fmul_rn(p, p);
-    p = __fmul_rn(p, p);
-    p = __fmul_rn(p, p);
-    float h;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(p));
-    float phi_cdf = x >= 0.0f ? 1.0f - h : h;
-    if (x < GELU_TAIL_X) phi_cdf = normcdf_tail_f32(x);
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * -0.72134752044448170368f));
-    return fmaf(x * 0.39894228040143267794f, e, phi_cdf);
+    const float h = normal_tail_f32(x);
+    const float phi_cdf = x >= 0.0f ? 1.0f - h : h;
+    const float e = ex2_approx(x * -GELU_HALF_LOG2E * x);
+    return fmaf(x * INV_SQRT_2PI, e, phi_cdf);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
