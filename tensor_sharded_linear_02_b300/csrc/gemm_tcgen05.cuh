@@ -126,7 +126,13 @@ struct GemmArgs {
     int k_blocks;        // BK-deep blocks per k-group (ceil)
     int k_groups;        // 1, or the shard count for per-shard partial outputs
     int m_tiles, n_tiles;  // pair tiles (PAIR_M x bn)
-    int num_units;       // m_tiles * n_tiles * k_groups (persistent kernel)
+    int group_m;         // persistent order: tiles walk groups of group_m tile rows,
+                         // row fastest within a group (L2 reuse, see decode_unit)
+    int num_units;       // work units of the persistent kernel
+    int full_units;      // units 0 .. full_units-1 are whole bn-wide tiles; each later
+                         // unit is one half (bn/2 columns) of the remaining tiles, so
+                         // that a last, partly filled round of tiles runs as half-width
+                         // tiles on up to twice as many pairs
     int split;           // pairs per cluster S (cluster kernel)
     void *out;           // [M, N] row-major
     int64_t out_group_stride;  // elements between k-group outputs
@@ -406,13 +412,37 @@ __device__ __forceinline__ void epilogue_gelu_grad(const CUtensorMap *tmC,
     }
 }
 
-__device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_tile, int &n_tile,
-                                            int &g) {
+// Unit u of the persistent kernel -> k-group g, pair-tile row m_tile, first
+// output column col0 and width bn of its tile.  Tiles are numbered group by
+// group: a group is group_m consecutive tile rows (fewer in the last one)
+// and walks its tile columns one after the other, the rows of a column
+// fastest; then the next group, then the next k-group.  The pairs run
+// consecutive units at the same time, so a round of P units touches about
+// group_m rows of A and P / group_m columns of B: with group_m ~ sqrt(P)
+// that is the fewest operand bytes a round can touch, and the round's
+// successor shares the group's rows of A (L2 reuse).  Units below
+// full_units are whole tiles, the rest are the two column halves of the
+// last tiles.  Neither the order nor halving changes any element's
+// accumulation order, so results do not depend on them.
+__device__ __forceinline__ void decode_unit(const GemmArgs &a, int u, int &m_tile, int &col0,
+                                            int &g, int &bn) {
+    int t = u, half = 0;
+    bn = a.bn;
+    if (u >= a.full_units) {
+        const int v = u - a.full_units;
+        t = a.full_units + (v >> 1);
+        half = v & 1;
+        bn = a.bn >> 1;
+    }
     const int tiles = a.m_tiles * a.n_tiles;
-    g = u / tiles;
-    const int t = u - g * tiles;
-    m_tile = t % a.m_tiles;
-    n_tile = t / a.m_tiles;
+    g = t / tiles;
+    const int r = t - g * tiles;
+    const int per_group = a.group_m * a.n_tiles;
+    const int grp = r / per_group;
+    const int in = r - grp * per_group;
+    const int rows = min(a.group_m, a.m_tiles - grp * a.group_m);
+    m_tile = grp * a.group_m + in % rows;
+    col0 = (in / rows) * a.bn + half * bn;
 }
 
 // ---------------------------------------------------------------------------
@@ -436,11 +466,11 @@ template <int MAXBN, bool A_MN = false, bool B_KM = false>
 __device__ __forceinline__ bool produce_kblocks(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                                 uint8_t *ring, SmemBarriers *bars,
                                                 uint32_t full_remote, bool leader, int half,
-                                                ProducerState &ps, int m_tile, int n_tile, int bn,
-                                                int g, int kb0, int kb1, uint64_t limit) {
+                                                ProducerState &ps, int m_tile, int tile_col0,
+                                                int bn, int g, int kb0, int kb1, uint64_t limit) {
     using R = Ring<MAXBN>;
     const int row0 = m_tile * PAIR_M + half * BM;
-    const int col0 = n_tile * bn + half * (bn / 2);
+    const int col0 = tile_col0 + half * (bn / 2);
     const int chunks = bn / 2 / B_CHUNK_N;
     const uint32_t tx = pair_stage_tx(bn);
     for (int kb = kb0; kb < kb1; ++kb) {
@@ -639,11 +669,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const bool leader = half == 0;
     const int pair = blockIdx.x >> 1;
     const int num_pairs = gridDim.x >> 1;
-    const int bn = a.bn;
 
     const CUtensorMap *maps[4] = {&tmA, &tmB, &tmC, &tmAux};
     gemm_setup(bars, R::STAGES, TMEM_COLS_PERSISTENT, maps,
-               EPI == EPI_DUAL ? 4 : (a.tma_store ? 3 : 2));
+               (EPI == EPI_DUAL || (B_KM && a.full_units < a.num_units)) ? 4
+                                                                         : (a.tma_store ? 3 : 2));
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(&bars->tmem_base);
     const uint64_t limit = a.wait_limit_ns;
 
@@ -653,10 +683,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ProducerState ps;
             bool ok = true;
             for (int u = pair; u < a.num_units && ok; u += num_pairs) {
-                int mt, nt, g;
-                decode_unit(a, u, mt, nt, g);
-                ok = produce_kblocks<MAXBN, A_MN, B_KM>(&tmA, &tmB, ring, bars, full_remote,
-                                                        leader, half, ps, mt, nt, bn, g, 0,
+                int mt, c0, g, bn;
+                decode_unit(a, u, mt, c0, g, bn);
+                // [N][K] B: the half-width units read boxes of half as many
+                // rows, through the second map (tmAux is otherwise unused there)
+                const CUtensorMap *mb = (B_KM && bn != a.bn) ? &tmAux : &tmB;
+                ok = produce_kblocks<MAXBN, A_MN, B_KM>(&tmA, mb, ring, bars, full_remote,
+                                                        leader, half, ps, mt, c0, bn, g, 0,
                                                         a.k_blocks, limit);
             }
             if (ok) ok = producer_tail<MAXBN>(bars, ps, limit);
@@ -665,11 +698,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (leader && lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(PAIR_M, bn, !B_KM, A_MN);
             int stage = 0, local = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int u = pair; u < a.num_units && ok; u += num_pairs, ++local) {
+                int mt, c0, g, bn;
+                decode_unit(a, u, mt, c0, g, bn);
+                const uint32_t idesc = idesc_bf16_f32(PAIR_M, bn, !B_KM, A_MN);
                 const int acc = local & 1;
                 const uint32_t acc_par = (local >> 1) & 1;
                 ok = mbar_wait_bounded(smem_u32(&bars->acc_empty[acc]), acc_par ^ 1u, limit,
@@ -687,7 +722,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
     } else {
         const int q = warp & 3;                         // TMEM lane quadrant
-        const int cofs = ((warp - 2) >> 2) * (bn / 2);  // this warp's half of the columns
+        const int chalf = (warp - 2) >> 2;              // this warp's half of the columns
         const uint32_t acc_empty_remote = dsmem_map(smem_u32(&bars->acc_empty[0]), 0);
         const uint32_t stg = smem_u32(staging + (warp - 2) * STG_BYTES);
         int local = 0;
@@ -698,22 +733,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 SITE_EPI_ACC_FULL))
                 break;
             tc_fence_after();
-            int mt, nt, g;
-            decode_unit(a, u, mt, nt, g);
+            int mt, c0, g, bn;
+            decode_unit(a, u, mt, c0, g, bn);
+            const int cofs = chalf * (bn / 2);
             const uint32_t taddr =
                 tmem_base + acc * ACC_STRIDE + (static_cast<uint32_t>(q * 32) << 16);
             const uint32_t release = acc_empty_remote + acc * 8;
             const int row0 = mt * PAIR_M + half * BM + q * 32;
             if constexpr (EPI == EPI_GELU_GRAD) {
-                epilogue_gelu_grad(&tmC, a.aux, a.M, a.N, taddr, stg, row0, nt * bn, cofs, bn / 2,
+                epilogue_gelu_grad(&tmC, a.aux, a.M, a.N, taddr, stg, row0, c0, cofs, bn / 2,
                                    release);
             } else if constexpr (EPI == EPI_DUAL) {
-                epilogue_dual(&tmC, &tmAux, taddr, stg, row0, nt * bn, cofs, bn / 2, release);
+                epilogue_dual(&tmC, &tmAux, taddr, stg, row0, c0, cofs, bn / 2, release);
             } else if (a.tma_store) {
                 epilogue_tma_store(&tmC, a.out_f32 != 0, a.act_gelu != 0, taddr, stg, row0,
-                                   nt * bn, cofs, bn / 2, g, release, a.bias, a.N);
+                                   c0, cofs, bn / 2, g, release, a.bias, a.N);
             } else {
-                epilogue_direct(a, taddr, row0 + lane, nt * bn, cofs, bn / 2, g, release);
+                epilogue_direct(a, taddr, row0 + lane, c0, cofs, bn / 2, g, release);
             }
         }
         if (lane == 0) bulk_wait_read0();  // every store box has left shared memory
@@ -793,7 +829,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 dsmem_map(smem_u32(&bars->full[0]), static_cast<uint32_t>(2 * p));
             ProducerState ps;
             if (!produce_kblocks<256>(&tmA, &tmB, ring, bars, full_remote, leader, half, ps, mt,
-                                      nt, BN, 0, kb0, kb1, limit) ||
+                                      nt * BN, BN, 0, kb0, kb1, limit) ||
                 !producer_tail<256>(bars, ps, limit))
                 producer_drain(ps);
         }

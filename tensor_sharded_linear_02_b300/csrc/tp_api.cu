@@ -268,6 +268,16 @@ struct GemmCall {
     const void *bias = nullptr;  // bf16 [N], added before the activation
 };
 
+// Tile rows per group of the persistent kernel's tile order (about the
+// square root of the 74 pairs that run at once; see decode_unit), and the
+// share of the 126 MB L2 that one operand may claim to stay resident.
+// Measured (4096 x 4096 x 16384 products): the column GEMM (A = 32 MB) is
+// fastest with all 16 tile rows in one group (A read once), the weight-
+// gradient product with A = 128 MB (64 tile rows) 23 % faster with groups
+// of 8 than with one group.
+constexpr int kGroupM = 8;
+constexpr int64_t kL2Budget = int64_t(48) << 20;
+
 // Launch plan of one GEMM: tile width, and split = 2 for the cluster split
 // kernel (two pairs per tile), 1 for the persistent kernel.
 struct GemmPlan {
@@ -290,7 +300,9 @@ int plan_override() {
 // Picks the plan with the smallest estimated time, in units of one k-block
 // of a 256-wide pair tile (128 deep, about 1024 tensor-core cycles):
 //   persistent, width bn: waves * k_blocks * (bn / 256) * overhead(bn) plus
-//       the exposed epilogue of the last tile (larger with GeLU);
+//       the exposed epilogue of the last tile (larger with GeLU); for the
+//       256-wide plan a last round that fills at most half of the pairs
+//       runs as 128-wide half tiles (`half_tail`) and counts 0.75;
 //   split over two pairs (256-wide, one wave of clusters): k_blocks / 2
 //       plus the exchange of the partial rows between the two pairs (64 KiB
 //       of fp32 per CTA through distributed shared memory) and the tail.
@@ -298,13 +310,17 @@ int plan_override() {
 // same issue work (MMA and TMA instructions per stage) and 3/4 of its
 // operand bytes; measured, it takes about 0.75 of the 256-wide time.
 GemmPlan plan_gemm(int64_t M, int64_t N, int k_blocks, int k_groups, bool allow_split, bool gelu,
-                   const DeviceInfo &dev) {
+                   bool half_tail, const DeviceInfo &dev) {
     const int64_t m_tiles = (M + PAIR_M - 1) / PAIR_M;
     const int64_t u256 = m_tiles * ((N + 255) / 256) * k_groups;
     const int64_t u128 = m_tiles * ((N + 127) / 128) * k_groups;
     const int64_t P = dev.max_pairs;
     const double tail = gelu ? 6.0 : 2.0;
-    const double c256 = static_cast<double>((u256 + P - 1) / P) * k_blocks + tail;
+    const int64_t rem256 = u256 % P;
+    const double rounds256 = static_cast<double>(u256 / P) +
+                             (rem256 == 0 ? 0.0
+                                          : (half_tail && u256 > P && 2 * rem256 <= P ? 0.75 : 1.0));
+    const double c256 = rounds256 * k_blocks + tail;
     const double c128 = static_cast<double>((u128 + P - 1) / P) * k_blocks * 0.5 * 1.5 + tail / 2;
     GemmPlan best;
     double cbest = c256;
@@ -341,7 +357,8 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     // transposed A and the dual / GeLU' epilogues use 256-wide tiles
     const bool plain = !c.a_mn && c.epi == EPI_PLAIN;
     const GemmPlan plan = plain ? plan_gemm(c.M, c.N, static_cast<int>((Kg + BK - 1) / BK),
-                                            c.k_groups, c.allow_split && !c.b_km, c.gelu, *dev)
+                                            c.k_groups, c.allow_split && !c.b_km, c.gelu,
+                                            true, *dev)
                                 : GemmPlan{256, 1};
     CUtensorMap tmA, tmB, tmAux;
     if (c.a_mn) {
@@ -396,8 +413,31 @@ tp_status launch_gemm(const GemmCall &c, cudaStream_t s) {
     a.m_tiles = static_cast<int>((c.M + PAIR_M - 1) / PAIR_M);
     a.n_tiles = static_cast<int>((c.N + a.bn - 1) / a.bn);
     const int64_t units = static_cast<int64_t>(a.m_tiles) * a.n_tiles * c.k_groups;
-    if (units > kInt32Max) return TP_ERR_SHAPE;
+    if (units > kInt32Max / 2) return TP_ERR_SHAPE;
     a.num_units = static_cast<int>(units);
+    a.full_units = a.num_units;
+    // tile order: when all of A (the k-group's rows x K) fits the L2 budget
+    // it stays resident while B streams past once, so the rows of a group
+    // are all of them; otherwise groups of kGroupM rows keep each round's
+    // operand footprint near its minimum
+    const int64_t a_bytes = static_cast<int64_t>(a.m_tiles) * PAIR_M * Kg * 2;
+    a.group_m = (a_bytes <= kL2Budget || a.m_tiles < kGroupM) ? a.m_tiles : kGroupM;
+    // A last round of 256-wide tiles that fills at most half of the pairs
+    // runs as twice as many 128-wide half tiles (each about 3/4 of a tile's
+    // time).  The [N][K] (transposed) B operand's tensor-map box is as tall
+    // as half a tile, so the half tiles read it through a second map, in the
+    // kernel's auxiliary map slot (unused by those kernels otherwise).
+    if (plan.split == 1 && a.bn == 256 && !(c.b_km && c.epi == EPI_DUAL) &&
+        a.num_units > dev->max_pairs) {
+        const int rem = a.num_units % dev->max_pairs;
+        if (rem > 0 && 2 * rem <= dev->max_pairs) {
+            a.full_units = a.num_units - rem;
+            a.num_units += rem;
+            if (c.b_km && !encode_3d_cached(&tmAux, c.B, c.K, c.N, 1, c.K * 2, c.N * c.K * 2,
+                                            BK_BOX, static_cast<uint32_t>(a.bn / 4), 1))
+                return TP_ERR_CUDA;
+        }
+    }
     a.out = c.out;
     a.out_group_stride = c.out_group_stride;
     a.out_f32 = c.out_f32 ? 1 : 0;
@@ -946,7 +986,7 @@ tp_status tp_shard_concat_grouped(const void *Ys, void *Y, int64_t rows, int64_t
     if (ncv > kInt32Max || rows > kInt32Max) return TP_ERR_SHAPE;
     if (rows == 0 || ncv == 0) return TP_OK;
     // boxes: the widest of 256, 128, ... columns dividing sw, rows to fill
-    // 16 KiB (at most 256)
+    // CAT_BOX_BYTES (at most 256)
     int box_cols = 256;
     while (box_cols > vec && sw % box_cols != 0) box_cols /= 2;
     int box_rows = static_cast<int>(CAT_BOX_BYTES / (box_cols * es));

@@ -232,3 +232,44 @@ def test_gelu_grad_epilogue_accuracy(tp, cuda_device):
     # where the terms do not cancel, the one-ulp bound holds on its own
     clear = np.abs(ref) >= 0.05 * scale
     assert np.all(ulps[clear & (np.abs(ref) >= 1e-30)] <= 1)
+
+
+def test_backward_half_width_last_round(tp, cuda_device):
+    """Input and weight gradients whose 256-wide tiles fill a few more than
+    one round of the GPU's CTA pairs: the last tiles run as half-width
+    units, for dX = dY.W^T through the second, half-height tensor map of
+    the [N][K] operand, and for dW = X^T.dY.  Against the oracle and bit
+    for bit against the all-128-wide plan."""
+    import os
+    import torch
+    P = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    mt = P // 8 + 1
+    M, K, N, n = 256 * mt - 21, 8 * 256, 264, 2   # dX [M, K]: 8 * mt tiles
+    xb = inputs.bf16_normal((M, K), inputs.stream_seed(83, 0), 1.0)
+    wb = inputs.bf16_normal((K, N), inputs.stream_seed(83, 1), 0.02)
+    gb = inputs.bf16_normal((M, N), inputs.stream_seed(83, 2), 1.0)
+    X, W, dY = (to_dev_bf16(b, cuda_device) for b in (xb, wb, gb))
+    rX, rW = oracle.column_linear_backward(*(oracle.bf16_to_f64(b) for b in (xb, wb, gb)), n)
+    outs = {}
+    for plan in ("256", "128"):
+        os.environ["TP_GEMM_PLAN"] = plan
+        try:
+            dX = torch.empty(M, K, dtype=torch.float32, device=cuda_device)
+            tp.tp_column_linear_backward(X, W, dY, dX, None, n_shards=n)
+        finally:
+            del os.environ["TP_GEMM_PLAN"]
+        assert tp.tp_get_device_status() == tp.TP_OK
+        assert_bf16_parity(dev_to_f64(dX), rX, f"dX, plan {plan}", out_bf16=False)
+        outs[plan] = dev_bits(dX)
+    np.testing.assert_array_equal(outs["256"], outs["128"])
+    # dW = X^T.dY [K', N'] with K' = 256 mt rows of tiles: X2 [M2, 256 mt], dY2 [M2, 8 * 256]
+    M2 = 520
+    x2 = inputs.bf16_normal((M2, 256 * mt), inputs.stream_seed(84, 0), 1.0)
+    g2 = inputs.bf16_normal((M2, 2048), inputs.stream_seed(84, 1), 1.0)
+    w2 = inputs.bf16_normal((256 * mt, 2048), inputs.stream_seed(84, 2), 0.02)
+    X2, dY2, W2 = (to_dev_bf16(b, cuda_device) for b in (x2, g2, w2))
+    _, rW2 = oracle.column_linear_backward(*(oracle.bf16_to_f64(b) for b in (x2, w2, g2)), 1)
+    dW = torch.empty(256 * mt, 2048, dtype=torch.float32, device=cuda_device)
+    tp.tp_column_linear_backward(X2, W2, dY2, None, dW, n_shards=1)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    assert_bf16_parity(dev_to_f64(dW), rW2, "dW, short last round", out_bf16=False)

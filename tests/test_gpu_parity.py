@@ -804,3 +804,69 @@ def test_sequence_parallel_combines(tp, cuda_device, n, Mb, d, f):
                                                       act="gelu"))
         _status_ok(tp)
         np.testing.assert_array_equal(dev_bits(Hi), dev_bits(Hg[i * Mb:(i + 1) * Mb]))
+
+
+def _pairs():
+    """CTA pairs of the persistent GEMM on this GPU (one per two SMs)."""
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
+
+
+def test_half_width_last_round(tp, cuda_device):
+    """A product whose 256-wide pair tiles fill a few more than one round
+    (tiles = pairs + r, 2r <= pairs): the last r tiles run as 2r half-width
+    units.  Against the oracle, and bit for bit against the all-128-wide
+    plan (same accumulation order per element), for the column GEMM with
+    bias and GeLU (TMA stores, and the per-thread stores of the shard-major
+    copy), the fused row GEMM and the per-shard fp32 partials."""
+    import torch
+    P = _pairs()
+    mt = P // 8 + 1                       # 8 column tiles per row of tiles
+    M, K, N, n = 256 * mt - 37, 264, 8 * 256, 4  # ragged last tile row
+    assert 8 * mt > P and 2 * (8 * mt - P) <= P
+    xb, wb = _bf16_inputs(M, K, N, seed=77)
+    bb = inputs.bf16_normal((N,), inputs.stream_seed(77, 5), 0.5)
+    X, W, b = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device), to_dev_bf16(bb, cuda_device)
+    Xd, Wd, bd = oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb), oracle.bf16_to_f64(bb)
+    ref_c, ref_s = oracle.column_linear(Xd, Wd, n, act="gelu", bias=bd)
+    outs = {}
+    for plan in ("256", "128"):
+        Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+        Ys = torch.empty(n, M, N // n, dtype=torch.bfloat16, device=cuda_device)
+        _with_plan(plan, lambda: tp.tp_column_linear_bias(X, W, b, Yc, None, n_shards=n,
+                                                          act="gelu"))
+        _with_plan(plan, lambda: tp.tp_column_linear_bias(X, W, b, None, Ys, n_shards=n,
+                                                          act="gelu"))
+        _status_ok(tp)
+        assert_bf16_parity(bf16_dev_to_f64(Yc), ref_c, f"column + bias + GeLU, plan {plan}")
+        assert_bf16_parity(bf16_dev_to_f64(Ys), ref_s, f"shard-major, plan {plan}")
+        outs[plan] = (dev_bits(Yc), dev_bits(Ys))
+    np.testing.assert_array_equal(outs["256"][0], outs["128"][0])
+    np.testing.assert_array_equal(outs["256"][1], outs["128"][1])
+    # row split: X2 [M, 2048] . W2 [2048, 2048], n = 8 shards, fused and as partials
+    x2 = inputs.bf16_normal((M, N), inputs.stream_seed(78, 0), 1.0)
+    w2 = inputs.bf16_normal((N, N), inputs.stream_seed(78, 1), 0.02)
+    X2, W2 = to_dev_bf16(x2, cuda_device), to_dev_bf16(w2, cuda_device)
+    ref_r, ref_p = oracle.row_linear(oracle.bf16_to_f64(x2), oracle.bf16_to_f64(w2), 8)
+    routs = {}
+    for plan in ("256", "128"):
+        Yr = torch.empty(M, N, dtype=torch.float32, device=cuda_device)
+        _with_plan(plan, lambda: tp.tp_row_linear(X2, W2, Yr, None, n_shards=8))
+        _status_ok(tp)
+        assert_bf16_parity(dev_to_f64(Yr), ref_r, f"row, plan {plan}", out_bf16=False)
+        routs[plan] = dev_bits(Yr)
+    np.testing.assert_array_equal(routs["256"], routs["128"])
+    # per-shard partials: one output per shard (k-group), so the units are
+    # row tiles x column tiles x shards; one row tile, 8 column tiles and
+    # P // 8 + 1 shards leave the same short last round
+    Mp = 256
+    kg = P // 8 + 1
+    x3 = inputs.bf16_normal((Mp, 8 * kg), inputs.stream_seed(79, 0), 1.0)
+    w3 = inputs.bf16_normal((8 * kg, N), inputs.stream_seed(79, 1), 0.05)
+    X3, W3 = to_dev_bf16(x3, cuda_device), to_dev_bf16(w3, cuda_device)
+    Pd = torch.empty(kg, Mp, N, dtype=torch.float32, device=cuda_device)
+    tp.tp_row_linear(X3, W3, None, Pd, n_shards=kg)
+    _status_ok(tp)
+    _, ref_p3 = oracle.row_linear(oracle.bf16_to_f64(x3), oracle.bf16_to_f64(w3), kg)
+    assert_bf16_parity(dev_to_f64(Pd), ref_p3, "per-shard partials, short last round",
+                       out_bf16=False)
