@@ -163,7 +163,7 @@ class ClockSampler:
     @staticmethod
     def _parse_smi(text, t0, t1):
         import datetime
-        rows, maxes, reasons = [], [], set()
+        rows, maxes, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in text.splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -178,13 +178,18 @@ class ClockSampler:
                 continue
             rows.append(mhz)
             maxes.append(mx)
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for name, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not rows:
             return None
         return {"sm_mhz": statistics.median(rows), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi"}
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None, "source": "nvidia-smi"}
 
     def summary(self):
         if getattr(self, "_smi_summary", None):
