@@ -104,6 +104,10 @@ def _load():
         lib.orc_row_linear_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64]
         lib.orc_mlp_block_backward.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
                                                _i64, _i64]
+        _i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.orc_mlp_block_backward_sampled.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
+                                                       _i64p, _i64, _i64p, _i64, _i64p, _i64,
+                                                       _dp, _dp, _dp]
         lib.orc_shard_reduce.argtypes = [_fp, _dp, _i64, _i64, _i64]
         lib.orc_shard_concat.argtypes = [_dp, _dp, _i64, _i64, _i64, _i64]
         lib.orc_allgather_rows.argtypes = [_dp, _dp, _i64, _i64, _i64]
@@ -297,6 +301,27 @@ def mlp_block_backward(X, W1, W2, dY, n_shards: int):
     _load().orc_mlp_block_backward(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dY), _ptr(dX), _ptr(dW1),
                                    _ptr(dW2), M, d, f, n_shards)
     return dX, dW1, dW2
+
+
+def mlp_block_backward_sampled(X, W1, W2, dY, n_shards: int, dx_rows, dw1_cols, dw2_rows):
+    """The MLP block's backward on sampled outputs (for checks at sizes whose
+    full fp64 backward is too slow): returns (dX[dx_rows, :],
+    dW1[:, dw1_cols], dW2[dw2_rows, :]), each value by the same chain rule
+    as mlp_block_backward, written per value."""
+    X, W1, W2, dY = _f64(X), _f64(W1), _f64(W2), _f64(dY)
+    M, d = X.shape
+    _, f = W1.shape
+    assert W2.shape == (f, d) and dY.shape == (M, d) and f % n_shards == 0
+    rx = np.ascontiguousarray(dx_rows, dtype=np.int64)
+    c1 = np.ascontiguousarray(dw1_cols, dtype=np.int64)
+    r2 = np.ascontiguousarray(dw2_rows, dtype=np.int64)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    dXs = np.empty((rx.size, d)); dW1s = np.empty((d, c1.size)); dW2s = np.empty((r2.size, d))
+    _load().orc_mlp_block_backward_sampled(_ptr(X), _ptr(W1), _ptr(W2), _ptr(dY), M, d, f,
+                                           n_shards, _ptr(rx, i64p), rx.size, _ptr(c1, i64p),
+                                           c1.size, _ptr(r2, i64p), r2.size, _ptr(dXs),
+                                           _ptr(dW1s), _ptr(dW2s))
+    return dXs, dW1s, dW2s
 
 
 def shard_reduce(P) -> np.ndarray:

@@ -547,3 +547,100 @@ void orc_seq_parallel_mlp_block(const double *Xs, const double *W1, const double
     orc_reduce_scatter_rows(P, Ys, n_shards, M, d);
     free(X); free(W1i); free(Hi); free(P);
 }
+
+/* ------------------------------------------------------------------------ */
+/* The MLP block's backward on sampled outputs, for checks at sizes whose   */
+/* full fp64 backward is too slow: rows `rx` of dX, columns `c1` of dW1 and */
+/* rows `r2` of dW2.  Each sampled value is the same chain rule as          */
+/* orc_mlp_block_backward, written per value (no matrix copies):             */
+/*   Z[r, j] = sum_k X[r, k] W1[k, j],  H = GeLU(Z),                         */
+/*   dZ[r, j] = GeLU'(Z[r, j]) * sum_c dY[r, c] W2[j, c],                    */
+/*   dW2[j, c] = sum_r H[r, j] dY[r, c],  dW1[k, j] = sum_r X[r, k] dZ[r, j], */
+/*   dX[r, k] = sum over shards i (ascending) of sum_{j in shard i}          */
+/*              dZ[r, j] W1[k, j].                                           */
+/* ------------------------------------------------------------------------ */
+static double z_at(const double *X, const double *W1, int64_t r, int64_t j, int64_t d,
+                   int64_t f)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; ++k)
+        acc += X[r * d + k] * W1[k * f + j];
+    return acc;
+}
+
+static double dz_at(const double *X, const double *W1, const double *W2, const double *dY,
+                    int64_t r, int64_t j, int64_t d, int64_t f)
+{
+    double dh = 0.0;
+    for (int64_t c = 0; c < d; ++c)
+        dh += dY[r * d + c] * W2[j * d + c];
+    return dh * orc_gelu_grad(z_at(X, W1, r, j, d, f));
+}
+
+void orc_mlp_block_backward_sampled(const double *X, const double *W1, const double *W2,
+                                    const double *dY, int64_t M, int64_t d, int64_t f,
+                                    int64_t n_shards, const int64_t *rx, int64_t nrx,
+                                    const int64_t *c1, int64_t nc1, const int64_t *r2,
+                                    int64_t nr2, double *dXs, double *dW1s, double *dW2s)
+{
+    const int64_t fs = f / n_shards;
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t s = 0; s < nrx; ++s) {           /* dX rows */
+        const int64_t r = rx[s];
+        double *dz = (double *)malloc(sizeof(double) * (size_t)(f > 0 ? f : 1));
+        /* Z[r, :] with k outer (rows of W1 read in order; each Z[r, j] is   */
+        /* still summed over k ascending), then dZ[r, j]                     */
+        for (int64_t j = 0; j < f; ++j)
+            dz[j] = 0.0;
+        for (int64_t k = 0; k < d; ++k) {
+            const double xk = X[r * d + k];
+            for (int64_t j = 0; j < f; ++j)
+                dz[j] += xk * W1[k * f + j];
+        }
+        for (int64_t j = 0; j < f; ++j) {
+            double dh = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dh += dY[r * d + c] * W2[j * d + c];
+            dz[j] = dh * orc_gelu_grad(dz[j]);
+        }
+        for (int64_t k = 0; k < d; ++k) {
+            double tot = 0.0;
+            for (int64_t i = 0; i < n_shards; ++i) {
+                double part = 0.0;
+                for (int64_t j = i * fs; j < (i + 1) * fs; ++j)
+                    part += dz[j] * W1[k * f + j];
+                tot += part;
+            }
+            dXs[s * d + k] = tot;
+        }
+        free(dz);
+    }
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t s = 0; s < nc1; ++s) {           /* dW1 columns */
+        const int64_t j = c1[s];
+        double *dz = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1));
+        for (int64_t r = 0; r < M; ++r)
+            dz[r] = dz_at(X, W1, W2, dY, r, j, d, f);
+        for (int64_t k = 0; k < d; ++k) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < M; ++r)
+                acc += X[r * d + k] * dz[r];
+            dW1s[k * nc1 + s] = acc;
+        }
+        free(dz);
+    }
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t s = 0; s < nr2; ++s) {           /* dW2 rows */
+        const int64_t j = r2[s];
+        double *h = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1));
+        for (int64_t r = 0; r < M; ++r)
+            h[r] = orc_gelu(z_at(X, W1, r, j, d, f));
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < M; ++r)
+                acc += h[r] * dY[r * d + c];
+            dW2s[s * d + c] = acc;
+        }
+        free(h);
+    }
+}

@@ -137,3 +137,43 @@ def test_standalone_reduce_sweep(tp, cuda_device):
         bound = (n - 1) * 2.0 ** -24 * abs_sum
         assert np.all(np.abs(got - ref) <= bound + 1e-30), f"reduce N={n}"
         np.testing.assert_array_equal(dev_bits(Yb), oracle.f64_to_bf16(got).view(np.int16))
+
+
+def test_gpt_mlp_backward_sampled(tp, cuda_device):
+    """Backward of the GPT-style MLP block at full size (X [4096, 4096],
+    W1 [4096, 16384], W2 [16384, 4096], N = 8; dY ~ N(0, 1)), as the bench
+    runs it: the GPU computes dX, dW1, dW2 whole; the fp64 oracle computes
+    dX on rows in every 256-row tile, dW1 on columns and dW2 on rows spread
+    over every 256-wide tile of theirs (first and last included).  Two calls
+    are bit-identical."""
+    import torch
+    dev = cuda_device
+    M, d, f, n = 4096, 4096, 16384, 8
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(6, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(6, 1), 0.02)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(6, 2), 0.02)
+    gb = inputs.bf16_normal((M, d), inputs.stream_seed(6, 3), 1.0)
+    X, W1, W2, dY = (to_dev_bf16(b, dev) for b in (xb, w1b, w2b, gb))
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(2):
+        dX = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=dev)
+        dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=dev)
+        tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+        outs.append((dX, dW1, dW2))
+    assert tp.tp_get_device_status() == tp.TP_OK
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    dX, dW1, dW2 = outs[0]
+    rx = _rows(M, 1, 61)            # dX rows: one in every 256-row tile
+    c1 = _rows(f, 1, 62)[::2]       # dW1 columns: every other 256-wide tile
+    r2 = _rows(f, 1, 63)[1::2]      # dW2 rows: the other tiles
+    sX, sW1, sW2 = oracle.mlp_block_backward_sampled(
+        *(oracle.bf16_to_f64(b) for b in (xb, w1b, w2b, gb)), n, rx, c1, r2)
+    assert_bf16_parity(bf16_dev_to_f64(dX[torch.from_numpy(rx).to(dev)]), sX, "dX sampled rows")
+    assert_bf16_parity(bf16_dev_to_f64(dW1[:, torch.from_numpy(c1).to(dev)]), sW1,
+                       "dW1 sampled columns")
+    assert_bf16_parity(bf16_dev_to_f64(dW2[torch.from_numpy(r2).to(dev)]), sW2,
+                       "dW2 sampled rows")

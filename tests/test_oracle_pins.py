@@ -518,6 +518,42 @@ def test_mlp_backward_against_finite_differences():
                 assert abs(float(np.sum(g * e)) - q) <= 1e-7 * max(1.0, abs(q))
 
 
+def test_sampled_mlp_backward_matches_full_and_finite_differences():
+    """The per-value backward oracle (for full-size checks) against the
+    matrix-level backward oracle on small shapes, every shard count, and a
+    few of its values against central differences of the forward oracle."""
+    rng = np.random.default_rng(21)
+    for M, d, f in [(5, 4, 8), (3, 6, 12), (7, 3, 6)]:
+        X = rng.standard_normal((M, d))
+        W1 = rng.standard_normal((d, f)) * 0.5
+        W2 = rng.standard_normal((f, d)) * 0.5
+        dY = rng.standard_normal((M, d))
+        for n in [k for k in (1, 2, 3, 4, 6) if f % k == 0]:
+            rX, rW1, rW2 = oracle.mlp_block_backward(X, W1, W2, dY, n)
+            rows = [0, M - 1, M // 2]
+            cols = [0, f - 1, f // 3]
+            rows2 = [f - 1, 0, f // 2]
+            sX, sW1, sW2 = oracle.mlp_block_backward_sampled(X, W1, W2, dY, n, rows, cols, rows2)
+            np.testing.assert_allclose(sX, rX[rows], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(sW1, rW1[:, cols], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(sW2, rW2[rows2], rtol=1e-12, atol=1e-12)
+    # independent of both: L = sum(Y * dY), dL/dX[r, k] by central differences
+    M, d, f = 4, 3, 6
+    X = rng.standard_normal((M, d)); W1 = rng.standard_normal((d, f)); W2 = rng.standard_normal((f, d))
+    dY = rng.standard_normal((M, d))
+    sX, sW1, sW2 = oracle.mlp_block_backward_sampled(X, W1, W2, dY, 2, [2], [4], [1])
+    h = 1e-6
+    def L(X_, W1_, W2_):
+        return float(np.sum(oracle.mlp_block(X_, W1_, W2_, 2) * dY))
+    for k in range(d):
+        E = np.zeros_like(X); E[2, k] = h
+        assert abs((L(X + E, W1, W2) - L(X - E, W1, W2)) / (2 * h) - sX[0, k]) < 1e-6
+        E1 = np.zeros_like(W1); E1[k, 4] = h
+        assert abs((L(X, W1 + E1, W2) - L(X, W1 - E1, W2)) / (2 * h) - sW1[k, 0]) < 1e-6
+        E2 = np.zeros_like(W2); E2[1, k] = h
+        assert abs((L(X, W1, W2 + E2) - L(X, W1, W2 - E2)) / (2 * h) - sW2[0, k]) < 1e-6
+
+
 def test_backward_pins_catch_planted_mistakes():
     """Gradients with a dropped GeLU' factor or a missing shard in the
     backward sum fail the finite-difference pin that the oracle passes."""
