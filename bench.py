@@ -79,11 +79,68 @@ def _peaks():
 
 # ------------------------------------------------------------- clocks ------
 
-class ClockSampler:
-    """Samples SM clock and throttle reasons of one GPU through NVML (read
-    only) every few milliseconds while running."""
+class _CtypesNVML:
+    """The few read-only NVML queries the clock sampler makes, called in
+    libnvidia-ml directly (for hosts without the pynvml module)."""
+    NVML_CLOCK_SM = 1
 
-    def __init__(self, torch_device, period_s: float = 0.005):
+    def __init__(self):
+        import ctypes
+        self._c = ctypes
+        self._lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self._lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self._reasons = getattr(self._lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _ok(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} returned {rc}")
+
+    def nvmlDeviceGetCount(self):
+        n = self._c.c_uint()
+        self._ok(self._lib.nvmlDeviceGetCount_v2(self._c.byref(n)), "nvmlDeviceGetCount_v2")
+        return n.value
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self._c.c_void_p()
+        self._ok(self._lib.nvmlDeviceGetHandleByIndex_v2(self._c.c_uint(i), self._c.byref(h)),
+                 "nvmlDeviceGetHandleByIndex_v2")
+        return h
+
+    def nvmlDeviceGetUUID(self, h):
+        buf = self._c.create_string_buffer(96)
+        self._ok(self._lib.nvmlDeviceGetUUID(h, buf, self._c.c_uint(96)), "nvmlDeviceGetUUID")
+        return buf.value.decode()
+
+    def _clock(self, fn, h, kind):
+        v = self._c.c_uint()
+        self._ok(fn(h, self._c.c_uint(kind), self._c.byref(v)), "clock query")
+        return v.value
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind):
+        return self._clock(self._lib.nvmlDeviceGetMaxClockInfo, h, kind)
+
+    def nvmlDeviceGetClockInfo(self, h, kind):
+        return self._clock(self._lib.nvmlDeviceGetClockInfo, h, kind)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self._c.c_ulonglong()
+        self._ok(self._reasons(h, self._c.byref(v)), "clock event reasons")
+        return v.value
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        v = self._c.c_uint()
+        self._ok(self._lib.nvmlDeviceGetPowerUsage(h, self._c.byref(v)), "nvmlDeviceGetPowerUsage")
+        return v.value
+
+
+class ClockSampler:
+    """Samples SM clock, throttle reasons and power of one GPU through NVML
+    (read only; the pynvml module, else libnvidia-ml through ctypes, else
+    nvidia-smi) every millisecond or so while running."""
+
+    def __init__(self, torch_device, period_s: float = 0.001):
         self.device, self.period = torch_device, period_s
         self.samples = []
         self._stop = threading.Event()
@@ -92,18 +149,28 @@ class ClockSampler:
 
     def __enter__(self):
         self._smi = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = self._handle_for(pynvml)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
-        except Exception as e:  # no NVML module: sample through nvidia-smi
-            self.error = repr(e)
-            self._start_smi()
+        errors = []
+        for make in (self._pynvml, _CtypesNVML):
+            try:
+                nv = make()
+                self._nv = nv
+                self._h = self._handle_for(nv)
+                self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self._h, nv.NVML_CLOCK_SM)
+                self.source = "nvml" if make is self._pynvml else "nvml (ctypes)"
+                self._thread = threading.Thread(target=self._run, daemon=True)
+                self._thread.start()
+                return self
+            except Exception as e:
+                errors.append(repr(e))
+        self.error = "; ".join(errors)  # no NVML: sample through nvidia-smi
+        self._start_smi()
         return self
+
+    @staticmethod
+    def _pynvml():
+        import pynvml
+        pynvml.nvmlInit()
+        return pynvml
 
     def _start_smi(self):
         import subprocess
@@ -143,7 +210,11 @@ class ClockSampler:
             try:
                 mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
                 reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                self.samples.append((mhz, reasons))
+                try:
+                    mw = nv.nvmlDeviceGetPowerUsage(self._h)
+                except Exception:
+                    mw = None
+                self.samples.append((mhz, reasons, mw))
             except Exception as e:
                 self.error = repr(e)
             time.sleep(self.period)
@@ -209,12 +280,16 @@ class ClockSampler:
             "hw_power_brake_slowdown": getattr(nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
         }
         seen = 0
-        for _, r in self.samples:
+        for _, r, _ in self.samples:
             seen |= int(r)
         reasons = sorted(k for k, bit in names.items() if seen & bit and k != "gpu_idle")
-        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+        power = [w / 1000.0 for _, _, w in self.samples if w is not None]
+        return {"sm_mhz": statistics.median(m for m, _, _ in self.samples),
+                "sm_mhz_min": min(m for m, _, _ in self.samples),
                 "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
-                "source": "nvml"}
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None,
+                "source": getattr(self, "source", "nvml")}
 
 
 # ------------------------------------------------------------ helpers ------
