@@ -469,7 +469,10 @@ def run_ours(args):
     if tp.tp_get_device_status() != tp.TP_OK:
         raise RuntimeError("device status error in the timed region")
 
-    # per-kernel attribution: the same two GEMM launches with an event between
+    # per-kernel attribution: the same two GEMM launches with an event between,
+    # after a pause that lets the power controller settle again (the timed
+    # loop has just drawn full power; the split should see the same clocks)
+    time.sleep(0.25)
     k1_ms, k2_ms = _kernel_split(tp, torch, X, W1, W2, H, Y, n, flush, stream, K)
     roofline = _gemm_roofline(args.workload, k1_ms, k2_ms, flops_k1, flops_k2, peaks)
 

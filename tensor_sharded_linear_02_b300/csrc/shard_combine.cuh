@@ -23,11 +23,10 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b) {
 
 // Streaming reduce through shared memory: a persistent kernel, one CTA per
 // SM.  The output is cut into chunks of `chunk` elements (a multiple of 8);
-// CTA b takes chunks b, b + grid, ...  For each chunk one thread issues the
-// bulk copies of every shard's chunk * 4 contiguous bytes of P_i, in pieces
-// of at most `piece` bytes (a multiple of 16), into a stage of a
+// CTA b takes chunks b, b + grid, ...  For each chunk one thread issues one
+// bulk copy per shard (chunk * 4 contiguous bytes of P_i) into a stage of a
 // RED_STAGES-deep ring in shared memory, all counted on the stage's `full`
-// barrier; the 256 consumer threads add the shards of 8 consecutive
+// barrier (cutting the copies into 4-32 KiB pieces measured the same); the 256 consumer threads add the shards of 8 consecutive
 // elements in ascending shard order in fp32 from shared memory and store 16
 // bytes of bf16 (or 32 of fp32), and each consumer warp releases the stage.
 // Large contiguous copies keep every DRAM page open for long runs, and the
@@ -41,7 +40,7 @@ constexpr int RED_SMEM_BYTES = RED_STAGES * RED_STAGE_BYTES + 128;
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(RED_THREADS, 1)
     shard_reduce_bulk_kernel(const float *__restrict__ P, void *__restrict__ Y, int64_t total,
-                             int n_shards, int chunk, uint32_t piece, uint64_t limit_ns,
+                             int n_shards, int chunk, uint64_t limit_ns,
                              const __nv_bfloat16 *__restrict__ bias, int64_t cols) {
     extern __shared__ __align__(128) uint8_t red_smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(red_smem + RED_STAGES * RED_STAGE_BYTES);
@@ -79,12 +78,9 @@ __global__ void __launch_bounds__(RED_THREADS, 1)
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(fb, bytes * static_cast<uint32_t>(n_shards));
                 const uint32_t dst = smem_u32(red_smem + stage * RED_STAGE_BYTES);
-                for (int i = 0; i < n_shards; ++i) {
-                    const uint32_t d0 = dst + static_cast<uint32_t>(i) * static_cast<uint32_t>(chunk) * 4u;
-                    const char *s0 = reinterpret_cast<const char *>(P + static_cast<int64_t>(i) * total + e0);
-                    for (uint32_t off = 0; off < bytes; off += piece)
-                        bulk_load(d0 + off, s0 + off, bytes - off < piece ? bytes - off : piece, fb);
-                }
+                for (int i = 0; i < n_shards; ++i)
+                    bulk_load(dst + static_cast<uint32_t>(i) * static_cast<uint32_t>(chunk) * 4u,
+                              P + static_cast<int64_t>(i) * total + e0, bytes, fb);
                 issued = true;
                 if (++stage == RED_STAGES) {
                     stage = 0;

@@ -533,12 +533,6 @@ int reduce_grid(int64_t work_items, int sm_count) {
     return static_cast<int>(blocks);
 }
 
-// Largest single bulk copy of the reduce's producer.
-uint32_t red_piece_bytes(int n) {
-    (void)n;
-    return RED_STAGE_BYTES;
-}
-
 template <bool BF16>
 tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_count,
                           const void *bias, int64_t cols, cudaStream_t s) {
@@ -557,9 +551,8 @@ tp_status launch_reduce_t(const float *P, void *Y, int64_t total, int n, int sm_
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const uint32_t piece = red_piece_bytes(n);
         if (cudaLaunchKernelEx(&cfg, shard_reduce_bulk_kernel<BF16>, P, Y, total, n, chunk,
-                               piece, wait_limit_ns(), b, cols) != cudaSuccess)
+                               wait_limit_ns(), b, cols) != cudaSuccess)
             return TP_ERR_CUDA;
         return launch_status();
     }
