@@ -870,3 +870,48 @@ def test_half_width_last_round(tp, cuda_device):
     _, ref_p3 = oracle.row_linear(oracle.bf16_to_f64(x3), oracle.bf16_to_f64(w3), kg)
     assert_bf16_parity(dev_to_f64(Pd), ref_p3, "per-shard partials, short last round",
                        out_bf16=False)
+
+
+# ------------------------------------------------------ concurrent streams --
+
+def test_concurrent_streams(tp, cuda_device):
+    """Independent calls on separate streams (MLP blocks of three shapes,
+    one of them on the cluster split path, and a standalone reduce) overlap
+    on the GPU and give the same bits as the same calls one after another:
+    the kernels share no state but the error word, and the host's
+    tensor-map cache is locked."""
+    import torch
+    cases = [(200, 256, 512, 2), (2048, 1024, 4096, 2), (384, 512, 1024, 8)]
+    jobs = []
+    for i, (M, d, f, n) in enumerate(cases):
+        xb = inputs.bf16_normal((M, d), inputs.stream_seed(40 + i, 0), 1.0)
+        w1b = inputs.bf16_normal((d, f), inputs.stream_seed(40 + i, 1), 0.02)
+        w2b = inputs.bf16_normal((f, d), inputs.stream_seed(40 + i, 2), 0.02)
+        X, W1, W2 = (to_dev_bf16(b, cuda_device) for b in (xb, w1b, w2b))
+        ws = torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16),
+                         dtype=torch.uint8, device=cuda_device)
+        Yser = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+        tp.tp_mlp_block(X, W1, W2, Yser, ws, n_shards=n)
+        jobs.append((X, W1, W2, n, Yser, (M, d, f)))
+    P = to_dev_f32(inputs.f32_normal((4, 512, 1024), 47), cuda_device)
+    Rser = torch.empty(512, 1024, dtype=torch.float32, device=cuda_device)
+    tp.tp_shard_reduce(P, Rser)
+    torch.cuda.synchronize()
+
+    streams = [torch.cuda.Stream(cuda_device) for _ in range(len(jobs) + 1)]
+    outs, wss = [], []
+    for X, W1, W2, n, Yser, (M, d, f) in jobs:
+        outs.append(torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=cuda_device))
+        wss.append(torch.empty(tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16),
+                               dtype=torch.uint8, device=cuda_device))
+    R = torch.full((512, 1024), float("nan"), dtype=torch.float32, device=cuda_device)
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for s, (X, W1, W2, n, _, _), Y, ws in zip(streams, jobs, outs, wss):
+            tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n, stream=s)
+        tp.tp_shard_reduce(P, R, stream=streams[-1])
+    torch.cuda.synchronize()
+    _status_ok(tp)
+    for (_, _, _, _, Yser, shape), Y in zip(jobs, outs):
+        np.testing.assert_array_equal(dev_bits(Y), dev_bits(Yser), err_msg=f"MLP {shape}")
+    np.testing.assert_array_equal(R.cpu().numpy().view(np.int32), Rser.cpu().numpy().view(np.int32))
