@@ -34,6 +34,11 @@ Also reported on the same line:
   cpu_baseline  the fp64 oracle on the host cores, on a sample of the
                 workload's rows
   clocks        SM clock and throttle reasons sampled during the timed region
+                (NVML refreshes about every 100 ms: `distinct_readings` says
+                how many different readings a short region saw)
+  sustained     context: the same step back to back for about a second; the
+                rate over its second half and the clocks it settles to (the
+                power cap), against the measured sustained bf16 peak
 
 --impl reference times the oracle (plain fp64 host C) on a bounded sample of
 the same workload, as the reference arm.
@@ -143,6 +148,7 @@ class ClockSampler:
     def __init__(self, torch_device, period_s: float = 0.001):
         self.device, self.period = torch_device, period_s
         self.samples = []
+        self.times = []
         self._stop = threading.Event()
         self._thread = None
         self.error = None
@@ -215,6 +221,7 @@ class ClockSampler:
                 except Exception:
                     mw = None
                 self.samples.append((mhz, reasons, mw))
+                self.times.append(time.perf_counter())
             except Exception as e:
                 self.error = repr(e)
             time.sleep(self.period)
@@ -284,12 +291,22 @@ class ClockSampler:
             seen |= int(r)
         reasons = sorted(k for k, bit in names.items() if seen & bit and k != "gpu_idle")
         power = [w / 1000.0 for _, _, w in self.samples if w is not None]
-        return {"sm_mhz": statistics.median(m for m, _, _ in self.samples),
-                "sm_mhz_min": min(m for m, _, _ in self.samples),
-                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
-                "power_w_median": statistics.median(power) if power else None,
-                "power_w_max": max(power) if power else None,
-                "source": getattr(self, "source", "nvml")}
+        # NVML publishes a new reading about every 100 ms: over a shorter
+        # window every sample may be the same, last published, reading
+        changes = [t for t, a, b in zip(self.times[1:], self.samples, self.samples[1:]) if a != b]
+        gaps = [b - a for a, b in zip(changes, changes[1:])]
+        out = {"sm_mhz": statistics.median(m for m, _, _ in self.samples),
+               "sm_mhz_min": min(m for m, _, _ in self.samples),
+               "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+               "distinct_readings": len(set(self.samples)),
+               "nvml_refresh_ms": round(1e3 * statistics.median(gaps), 1) if gaps else None,
+               "power_w_median": statistics.median(power) if power else None,
+               "power_w_max": max(power) if power else None,
+               "source": getattr(self, "source", "nvml")}
+        if out["distinct_readings"] == 1:
+            out["note"] = ("one NVML reading throughout: NVML refreshes about every 100 ms, so "
+                           "the values are its last reading before or within this window")
+        return out
 
 
 # ------------------------------------------------------------ helpers ------
@@ -480,6 +497,16 @@ def run_ours(args):
     Ke = min(K, 200) if not args.skip_extras else 3
     e2e_ms, copy_us = run_e2e(tp, torch, xb, W1, W2, ws, M, d, n, Ke, stream)
 
+    # ---------------------------------------------------------- sustained ----
+    # context, not the headline: the same step back to back for about a
+    # second, the clocks the power controller settles to under continuous
+    # load (the timed region above is a burst of K steps)
+    sustained = None
+    if not args.skip_extras:
+        sustained = run_sustained(torch, dev, step, flush, stream, flops_step,
+                                  ms_per_step_hint=dev_ms / K, peaks=peaks)
+        time.sleep(0.5)
+
     # ------------------------------------------------------------- extras ----
     red = cat = bwd = others = small = None
     if not args.skip_extras:
@@ -549,11 +576,42 @@ def run_ours(args):
         "gpu_launches": 2 * K,  # the timed region: two GEMM launches per step
         "cpu_baseline": cpu,
         "clocks": clocks,
+        "sustained": sustained,
         "wall_s_timed_loop": round(t_wall, 3),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_sustained(torch, dev, step, flush, stream, flops_step, ms_per_step_hint, peaks,
+                  seconds=1.0):
+    """The step (L2 flushed before each) back to back for about `seconds`,
+    with CUDA events per step and the clock sampler running; reports the
+    rate over the last half (after the power controller has settled) and
+    the clocks seen."""
+    n = max(20, int(seconds * 1e3 / max(ms_per_step_hint, 1e-3)))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        for i in range(n):
+            _prequeue(torch, i)
+            _flush_l2(flush)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    first = sum(ms[:20]) / 20
+    late = sum(ms[n // 2:]) / (n - n // 2)
+    tf = flops_step / (late * 1e-3) / 1e12
+    sus = peaks.get("bf16_tflops_sustained")
+    return {"steps": n, "ms_per_step_first20": round(first, 5),
+            "ms_per_step_second_half": round(late, 5), "value_second_half": round(tf, 2),
+            "unit": "TFLOP/s",
+            "frac_of_sustained_peak": round(tf / sus, 4) if sus else None,
+            "sustained_peak": sus, "clocks": clk.summary()}
 
 
 def bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=2000):
