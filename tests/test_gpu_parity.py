@@ -915,3 +915,53 @@ def test_concurrent_streams(tp, cuda_device):
     for (_, _, _, _, Yser, shape), Y in zip(jobs, outs):
         np.testing.assert_array_equal(dev_bits(Y), dev_bits(Yser), err_msg=f"MLP {shape}")
     np.testing.assert_array_equal(R.cpu().numpy().view(np.int32), Rser.cpu().numpy().view(np.int32))
+
+
+# ------------------------------------------------------- random shapes ------
+
+def _random_shapes(count, seed):
+    """Seeded shapes inside the boundary's rules (rows of 16-byte multiples,
+    shard widths and depths multiples of 8), from one row up to a few tiles
+    with ragged tails; n from {1, 2, 3, 4, 8}."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        n = int(rng.choice([1, 2, 3, 4, 8]))
+        M = int(rng.integers(1, 700))
+        K = 8 * n * int(rng.integers(1, max(2, 1100 // (8 * n))))
+        N = 8 * n * int(rng.integers(1, max(2, 1100 // (8 * n))))
+        out.append((M, K, N, n))
+    return out
+
+
+@pytest.mark.parametrize("M,K,N,n", _random_shapes(8, 20261203))
+def test_random_shapes(tp, cuda_device, M, K, N, n):
+    """Column GEMM (with GeLU), row GEMM with the fused shard sum and the
+    MLP block (d = K, f = N) on seeded random shapes, each against the
+    oracle; the column output also bit for bit against the unsharded
+    launch."""
+    import torch
+    seed = 7 * M + 3 * K + N + n
+    xb, wb = _bf16_inputs(M, K, N, seed=seed)
+    X, W = to_dev_bf16(xb, cuda_device), to_dev_bf16(wb, cuda_device)
+    Xd, Wd = oracle.bf16_to_f64(xb), oracle.bf16_to_f64(wb)
+    Yc = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    Yc1 = torch.empty_like(Yc)
+    tp.tp_column_linear(X, W, Yc, None, n_shards=n, act="gelu")
+    tp.tp_column_linear(X, W, Yc1, None, n_shards=1, act="gelu")
+    Yr = torch.empty(M, N, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_row_linear(X, W, Yr, None, n_shards=n)
+    w2b = inputs.bf16_normal((N, K), inputs.stream_seed(seed, 2), 0.02)
+    W2 = to_dev_bf16(w2b, cuda_device)
+    Ym = torch.empty(M, K, dtype=torch.bfloat16, device=cuda_device)
+    ws = torch.empty(tp.tp_mlp_block_workspace_size(M, N, torch.bfloat16), dtype=torch.uint8,
+                     device=cuda_device)
+    tp.tp_mlp_block(X, W, W2, Ym, ws, n_shards=n)
+    _status_ok(tp)
+    ref_c, _ = oracle.column_linear(Xd, Wd, n, act="gelu")
+    assert_bf16_parity(bf16_dev_to_f64(Yc), ref_c, f"column {M}x{K}x{N} n={n}")
+    np.testing.assert_array_equal(dev_bits(Yc), dev_bits(Yc1))
+    ref_r, _ = oracle.row_linear(Xd, Wd, n)
+    assert_bf16_parity(bf16_dev_to_f64(Yr), ref_r, f"row {M}x{K}x{N} n={n}")
+    ref_m = oracle.mlp_block(Xd, Wd, oracle.bf16_to_f64(w2b), n)
+    assert_bf16_parity(bf16_dev_to_f64(Ym), ref_m, f"MLP {M}x{K}x{N} n={n}")
