@@ -273,3 +273,51 @@ def test_backward_half_width_last_round(tp, cuda_device):
     tp.tp_column_linear_backward(X2, W2, dY2, None, dW, n_shards=1)
     assert tp.tp_get_device_status() == tp.TP_OK
     assert_bf16_parity(dev_to_f64(dW), rW2, "dW, short last round", out_bf16=False)
+
+
+def _random_backward_shapes(count, seed):
+    """Seeded shapes inside the boundary's rules (dimensions that are row
+    pitches multiples of 8; the split axis a multiple of 8 n), one row up to
+    a few tiles with ragged tails."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        n = int(rng.choice([1, 2, 3, 4, 8]))
+        M = int(rng.integers(1, 600))
+        d = 8 * int(rng.integers(1, 90))
+        f = 8 * n * int(rng.integers(1, max(2, 900 // (8 * n))))
+        out.append((M, d, f, n))
+    return out
+
+
+@pytest.mark.parametrize("M,d,f,n", _random_backward_shapes(6, 20261204))
+def test_random_shapes_backward(tp, cuda_device, M, d, f, n):
+    """The MLP block's gradients and the row linear's (X = H-like input of
+    width f, W = W2) on seeded random shapes, each against the oracle."""
+    import torch
+    seed = 11 * M + 5 * d + f + n
+    xb = inputs.bf16_normal((M, d), inputs.stream_seed(seed, 0), 1.0)
+    w1b = inputs.bf16_normal((d, f), inputs.stream_seed(seed, 1), 0.02)
+    w2b = inputs.bf16_normal((f, d), inputs.stream_seed(seed, 2), 0.02)
+    gb = inputs.bf16_normal((M, d), inputs.stream_seed(seed, 3), 1.0)
+    hb = inputs.bf16_normal((M, f), inputs.stream_seed(seed, 4), 0.5)
+    X, W1, W2, dY, Hx = (to_dev_bf16(b, cuda_device) for b in (xb, w1b, w2b, gb, hb))
+    ws = torch.empty(tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16),
+                     dtype=torch.uint8, device=cuda_device)
+    dX = torch.empty(M, d, dtype=torch.bfloat16, device=cuda_device)
+    dW1 = torch.empty(d, f, dtype=torch.bfloat16, device=cuda_device)
+    dW2 = torch.empty(f, d, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+    dH = torch.empty(M, f, dtype=torch.bfloat16, device=cuda_device)
+    dWr = torch.empty(f, d, dtype=torch.bfloat16, device=cuda_device)
+    tp.tp_row_linear_backward(Hx, W2, dY, dH, dWr, n_shards=n)
+    assert tp.tp_get_device_status() == tp.TP_OK
+    f64 = oracle.bf16_to_f64
+    rX, rW1, rW2 = oracle.mlp_block_backward(f64(xb), f64(w1b), f64(w2b), f64(gb), n)
+    shape = f"{M}x{d}x{f} n={n}"
+    assert_bf16_parity(bf16_dev_to_f64(dX), rX, f"MLP dX {shape}")
+    assert_bf16_parity(bf16_dev_to_f64(dW1), rW1, f"MLP dW1 {shape}")
+    assert_bf16_parity(bf16_dev_to_f64(dW2), rW2, f"MLP dW2 {shape}")
+    rH, rWr = oracle.row_linear_backward(f64(hb), f64(w2b), f64(gb), n)
+    assert_bf16_parity(bf16_dev_to_f64(dH), rH, f"row dX {shape}")
+    assert_bf16_parity(bf16_dev_to_f64(dWr), rWr, f"row dW {shape}")
