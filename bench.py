@@ -18,8 +18,10 @@ Also reported on the same line:
   roofline      the dominant kernel of the step (per-kernel event timing of
                 the same two launches) against the measured bf16 burst peak,
                 with its DRAM bytes per launch from the committed capture
-  mlp_small     the small MLP block (2048 x 1024 x 4096, N = 2): block time,
-                per-kernel split and roofline
+  mlp_small     the small MLP block (2048 x 1024 x 4096, N = 2): block time
+                (L2 flushed before each block), per-kernel split and roofline;
+                `streamed`: blocks back to back over input sets five times
+                the L2 (cold operands, no flush), one event pair
   reduce        the standalone shard reduce, N = 8 fp32 partials
                 [8, 4096, 8192] -> bf16 (1.14 GB per launch, larger than L2),
                 and its sweep over N = 1, 2, 4, 8, 16
@@ -511,6 +513,7 @@ def run_ours(args):
     red = cat = bwd = others = small = None
     if not args.skip_extras:
         small = bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=min(max(K, 200), 2000))
+        small["streamed"] = bench_mlp_small_stream(tp, torch, dev, stream, peaks)
         red = bench_reduce(tp, dev, stream, peaks, K=min(K, 200))
         red["sweep"] = {str(ns): bench_reduce(tp, dev, stream, peaks, K=min(K, 100), n=ns)["value"]
                         for ns in (1, 2, 4, 16)}
@@ -612,6 +615,56 @@ def run_sustained(torch, dev, step, flush, stream, flops_step, ms_per_step_hint,
             "unit": "TFLOP/s",
             "frac_of_sustained_peak": round(tf / sus, 4) if sus else None,
             "sustained_peak": sus, "clocks": clk.summary()}
+
+
+def bench_mlp_small_stream(tp, torch, dev, stream, peaks, sets=16, K=400):
+    """The small MLP block run back to back over `sets` independent input
+    sets (X, W1, W2, Y and workspace: 40 MB each, 16 sets = 5 times the
+    126 MB L2), step i on set i mod sets, so every step finds its operands
+    cold in L2 without a flush (the other sets have passed through it
+    since), as consecutive layers with their own weights would.  One event pair around
+    the K steps: the launches of consecutive blocks overlap through
+    programmatic dependent launch, as they would in a model."""
+    name = "mlp_2048x1024x4096_n2"
+    M, d, f, n, std = WORKLOADS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(20261203)
+
+    def bf(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    wsb = tp.tp_mlp_block_workspace_size(M, f, torch.bfloat16)
+    sets_ = [(bf(M, d), bf(d, f, s=std), bf(f, d, s=std),
+              torch.empty(M, d, dtype=torch.bfloat16, device=dev),
+              torch.empty(wsb, dtype=torch.uint8, device=dev)) for _ in range(sets)]
+    set_bytes = sum(t.numel() * t.element_size() for t in sets_[0])
+
+    def step(i):
+        X, W1, W2, Y, ws = sets_[i % sets]
+        tp.tp_mlp_block(X, W1, W2, Y, ws, n_shards=n)
+
+    for i in range(2 * sets):
+        step(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(PREQUEUE_SLEEP_CYCLES)  # the host enqueues while the GPU waits
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the streamed small MLP blocks")
+    ms = e0.elapsed_time(e1) / K
+    tf = 2 * 2.0 * M * d * f / (ms * 1e-3) / 1e12
+    del sets_
+    return {"workload": name, "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "steps": K, "sets": sets, "bytes_all_sets": sets * set_bytes,
+            "l2": "not flushed: step i uses input set i mod sets, all sets together "
+                  "several times the L2, so each step's operands are cold",
+            "timing": "one event pair around the K steps (consecutive blocks overlap "
+                      "their launch costs through programmatic dependent launch)"}
 
 
 def bench_mlp_small(tp, torch, dev, stream, flush, peaks, K=2000):
