@@ -525,6 +525,7 @@ def run_ours(args):
                                       "mlp_4096x4096x16384_n8", K=min(K, 20))
         bwd_small = bench_backward_workload(tp, torch, dev, stream, flush, peaks,
                                             "mlp_2048x1024x4096_n2", K=min(max(K, 100), 500))
+        bwd_small["streamed"] = bench_backward_small_stream(tp, torch, dev, stream, peaks)
         bwd = {"mlp_4096x4096x16384_n8": bwd, "mlp_2048x1024x4096_n2": bwd_small}
         others = bench_other_workloads(tp, torch, dev, stream, flush, peaks, K=min(K, 20))
 
@@ -903,6 +904,54 @@ def bench_backward_workload(tp, torch, dev, stream, flush, peaks, name, K=20):
             "per_launch": per,
             "note": "dX, dW1, dW2 (bf16) with the pre-activation recomputed; L2 flushed "
                     "before every step; counted work excludes the recomputation"}
+
+
+def bench_backward_small_stream(tp, torch, dev, stream, peaks, sets=8, K=200):
+    """tp_mlp_block_backward on the small MLP run back to back over `sets`
+    independent input sets (92 MB each with workspace and gradients; 8 sets
+    = 5.8 times the L2), step i on set i mod sets, one event pair around the
+    K steps (cold operands without a flush; the launches of consecutive
+    steps overlap through programmatic dependent launch)."""
+    name = "mlp_2048x1024x4096_n2"
+    M, d, f, n, std = WORKLOADS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(20261204)
+
+    def bf(*shape, s=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * s).to(torch.bfloat16)
+
+    wsb = tp.tp_mlp_block_backward_workspace_size(M, f, torch.bfloat16)
+    sets_ = []
+    for _ in range(sets):
+        sets_.append((bf(M, d), bf(d, f, s=std), bf(f, d, s=std), bf(M, d),
+                      torch.empty(wsb, dtype=torch.uint8, device=dev),
+                      torch.empty(M, d, dtype=torch.bfloat16, device=dev),
+                      torch.empty(d, f, dtype=torch.bfloat16, device=dev),
+                      torch.empty(f, d, dtype=torch.bfloat16, device=dev)))
+
+    def step(i):
+        X, W1, W2, dY, ws, dX, dW1, dW2 = sets_[i % sets]
+        tp.tp_mlp_block_backward(X, W1, W2, dY, ws, dX, dW1, dW2, n_shards=n)
+
+    for i in range(2 * sets):
+        step(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(PREQUEUE_SLEEP_CYCLES)
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if tp.tp_get_device_status() != tp.TP_OK:
+        raise RuntimeError("device status error in the streamed backward steps")
+    ms = e0.elapsed_time(e1) / K
+    tf = 4 * 2.0 * M * d * f / (ms * 1e-3) / 1e12
+    del sets_
+    return {"value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "steps": K, "sets": sets,
+            "l2": "not flushed: input sets together several times the L2",
+            "timing": "one event pair around the K steps"}
 
 
 def _time_steps(torch, step, flush, stream, K):
